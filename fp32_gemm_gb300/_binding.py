@@ -1,0 +1,266 @@
+"""ctypes binding of the gx_gemm C ABI (include/sdm_gx_gemm.h). Argument marshalling only: torch tensors are turned
+into device pointers, element strides and the current CUDA stream; every step of the update runs in the library's
+kernels. There is no CPU fallback: if the library is not built, importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm.so")
+
+FLAG_GENERIC = 0x100
+FLAG_NO_PREFETCH = 0x200
+FLAG_CONFIG_MASK = 0x0FF
+FLAG_CTAS_SHIFT = 12
+
+STATUS = {
+    0: "SDM_GX_OK", -1: "SDM_GX_E_NULL", -2: "SDM_GX_E_SHAPE", -3: "SDM_GX_E_RANGE", -4: "SDM_GX_E_ALIGN",
+    -5: "SDM_GX_E_OVERLAP", -6: "SDM_GX_E_STRIDE", -7: "SDM_GX_E_GRID", -8: "SDM_GX_E_SMEM", -9: "SDM_GX_E_DEVICE",
+    -10: "SDM_GX_E_PLAN", -11: "SDM_GX_E_PLAN_TI", -12: "SDM_GX_E_PLAN_DEVICE", -13: "SDM_GX_E_FLAGS",
+    -14: "SDM_GX_E_CUDA", -15: "SDM_GX_E_DEVICE_FAULT", -16: "SDM_GX_E_UNSUPPORTED", -17: "SDM_GX_E_ALLOC",
+}
+CODE = {v: k for k, v in STATUS.items()}
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("x_sn", ctypes.c_int64), ("x_sj", ctypes.c_int64), ("dv_sn", ctypes.c_int64),
+                ("dv_sj", ctypes.c_int64), ("du_sn", ctypes.c_int64), ("du_si", ctypes.c_int64)]
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("config", ctypes.c_int32), ("TI", ctypes.c_int32),
+                ("TC", ctypes.c_int32), ("KB", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("tiles", ctypes.c_int64),
+                ("ctas", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32), ("sms", ctypes.c_int32),
+                ("one_wave", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: int(getattr(self, k)) for k, _ in self._fields_}
+
+
+class GxGemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        self.name = STATUS.get(self.status, str(status))
+        msg = f"{where}: {self.name} ({_lib.sdm_gx_strerror(status).decode()})"
+        if self.status == CODE["SDM_GX_E_CUDA"]:
+            msg += f" [cudaError {_lib.sdm_gx_last_cuda_error()}]"
+        super().__init__(msg)
+
+
+SIGNATURES = {
+    # name: (restype, argtypes)
+    "sdm_gx_gemm_step": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 + [ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_step_ex": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 5 +
+                            [ctypes.POINTER(Strides), ctypes.c_void_p, ctypes.c_int, ctypes.c_uint]),
+    "sdm_gx_gemm_geometry": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
+                             [ctypes.POINTER(Strides), ctypes.c_uint, ctypes.POINTER(Geom)]),
+    "sdm_gx_gemm_plan_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p)] + [ctypes.c_void_p] * 3 +
+                                [ctypes.c_int64] * 4 + [ctypes.POINTER(Strides), ctypes.c_int64, ctypes.c_uint]),
+    "sdm_gx_gemm_plan_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_plan_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_int]),
+    "sdm_gx_gemm_plan_run_producer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                     ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_plan_geometry": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Geom)]),
+    "sdm_gx_gemm_plan_destroy": (None, [ctypes.c_void_p]),
+    "sdm_gx_producer_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 4 +
+                             [ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_kernel_attrs": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]),
+    "sdm_gx_gemm_num_configs": (ctypes.c_int, [ctypes.c_int32]),
+    "sdm_gx_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "sdm_gx_launch_counts": (None, [ctypes.POINTER(ctypes.c_int64)]),
+    "sdm_gx_last_cuda_error": (ctypes.c_int, []),
+    "sdm_gx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "sdm_gx_abi_version": (ctypes.c_int, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"gx_gemm CUDA library not built ({LIB_PATH} missing): run fp32_gemm_gb300.build.build() "
+                          "or __graft_entry__.build(); there is no CPU fallback")
+    L = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise GxGemmError(rc, where)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _as3(t: torch.Tensor, rows: int, cols: int, N: int) -> torch.Tensor:
+    """A [N, rows, cols] view of a float32 CUDA tensor with unit innermost stride (no copy)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32:
+        raise TypeError("gx_gemm: operands are float32 CUDA tensors")
+    if t.is_neg() or t.is_conj():
+        raise TypeError("gx_gemm: lazy negative / conjugate views are not supported (materialise them first)")
+    if t.dim() == 3:
+        v = t
+    elif t.dim() == 2 and t.shape[0] == N * rows:
+        v = t.view(N, rows, cols) if t.is_contiguous() else t.unflatten(0, (N, rows))
+    else:
+        raise ValueError(f"gx_gemm: expected [N, {rows}, {cols}] (or [N*{rows}, {cols}]), got {tuple(t.shape)}")
+    if tuple(v.shape) != (N, rows, cols):
+        raise ValueError(f"gx_gemm: expected shape {(N, rows, cols)}, got {tuple(v.shape)}")
+    if v.stride(2) != 1:
+        raise ValueError("gx_gemm: the innermost stride must be 1")
+    return v
+
+
+def _operands(d_u, x, d_dv):
+    if x.dim() != 3:
+        raise ValueError("gx_gemm: x is [N, C, C]")
+    N, C = int(x.shape[0]), int(x.shape[1])
+    hd = int(d_u.shape[-1])
+    xv = _as3(x, C, C, N)
+    uv = _as3(d_u, C, hd, N)
+    vv = _as3(d_dv, C, hd, N)
+    s = Strides(xv.stride(0), xv.stride(1), vv.stride(0), vv.stride(1), uv.stride(0), uv.stride(1))
+    return uv, xv, vv, N, C, hd, s
+
+
+def step(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, stream=None) -> None:
+    """sdm_gx_gemm_step: one step on contiguous operands (d_u updated in place)."""
+    if not (d_u.is_contiguous() and x.is_contiguous() and d_dv.is_contiguous()):
+        raise ValueError("gx_gemm.step: contiguous operands (use step_ex for strided views)")
+    C = int(x.shape[1])
+    hd = int(d_u.shape[-1])
+    _check(_lib.sdm_gx_gemm_step(d_u.data_ptr(), x.data_ptr(), d_dv.data_ptr(), int(ti), int(P), C, hd,
+                                 _stream(stream), int(bool(pdl))), "sdm_gx_gemm_step")
+
+
+def step_ex(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, flags: int = 0, stream=None) -> None:
+    """sdm_gx_gemm_step_ex: one step on strided [N, ...] operands."""
+    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    _check(_lib.sdm_gx_gemm_step_ex(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), int(ti), N, int(P), C, hd,
+                                    ctypes.byref(s), _stream(stream), int(bool(pdl)), int(flags)),
+           "sdm_gx_gemm_step_ex")
+
+
+def geometry(d_u, x, d_dv, P: int, flags: int = 0) -> dict:
+    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    g = Geom()
+    _check(_lib.sdm_gx_gemm_geometry(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd,
+                                     ctypes.byref(s), int(flags), ctypes.byref(g)), "sdm_gx_gemm_geometry")
+    return g.as_dict()
+
+
+class Plan:
+    """sdm_gx_gemm_plan_*: validated once, launched per step with only ti changing. Keeps references to the tensors
+    so that their memory outlives the plan."""
+
+    def __init__(self, d_u, x, d_dv, P: int, ti_max: int | None = None, flags: int = 0):
+        uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+        self._keep = (d_u, x, d_dv)
+        self.N, self.P, self.C, self.hd = N, int(P), C, hd
+        self.T = N // int(P) if P >= 1 else 0
+        self.ti_max = self.T - 1 if ti_max is None else int(ti_max)
+        h = ctypes.c_void_p()
+        _check(_lib.sdm_gx_gemm_plan_create(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
+                                            int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags)),
+               "sdm_gx_gemm_plan_create")
+        self._h = h
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    def step(self, ti: int, pdl: bool = False, stream=None) -> None:
+        _check(_lib.sdm_gx_gemm_plan_step(self._h, int(ti), _stream(stream), int(bool(pdl))),
+               "sdm_gx_gemm_plan_step")
+
+    def run(self, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, stream=None) -> None:
+        """Steps ti_begin, ti_begin +- 1, ... stopping before ti_end (default: all steps ascending)."""
+        ti_end = self.T if ti_end is None else int(ti_end)
+        _check(_lib.sdm_gx_gemm_plan_run(self._h, int(ti_begin), ti_end, _stream(stream), int(bool(pdl))),
+               "sdm_gx_gemm_plan_run")
+
+    def run_producer(self, S, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, stream=None) -> None:
+        """The chain with the synthetic producer before every step (d_dv(ti) = +-S(ti))."""
+        if not (S.is_cuda and S.dtype == torch.float32 and S.is_contiguous() and S.numel() == self.N * self.C * self.hd):
+            raise ValueError("run_producer: S is a contiguous float32 CUDA tensor shaped like d_dv")
+        ti_end = self.T if ti_end is None else int(ti_end)
+        self._keep_s = S
+        _check(_lib.sdm_gx_gemm_plan_run_producer(self._h, S.data_ptr(), int(ti_begin), ti_end, _stream(stream),
+                                                  int(bool(pdl))), "sdm_gx_gemm_plan_run_producer")
+
+    def geometry(self) -> dict:
+        g = Geom()
+        _check(_lib.sdm_gx_gemm_plan_geometry(self._h, ctypes.byref(g)), "sdm_gx_gemm_plan_geometry")
+        return g.as_dict()
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.sdm_gx_gemm_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001
+            pass
+
+
+def producer_step(d_dv, S, ti: int, P: int, pdl: bool = False, stream=None) -> None:
+    """sdm_gx_producer_step: d_dv(ti) = S(ti), negated for odd ti (contiguous [N, C, hd])."""
+    if not (d_dv.is_contiguous() and S.is_contiguous() and d_dv.shape == S.shape):
+        raise ValueError("producer_step: contiguous d_dv and S of one shape")
+    C, hd = int(d_dv.shape[-2]), int(d_dv.shape[-1])
+    _check(_lib.sdm_gx_producer_step(d_dv.data_ptr(), S.data_ptr(), int(ti), int(P), C, hd, _stream(stream),
+                                     int(bool(pdl))), "sdm_gx_producer_step")
+
+
+def kernel_attrs(path: int, config: int) -> dict:
+    out = (ctypes.c_int64 * 4)()
+    _check(_lib.sdm_gx_gemm_kernel_attrs(int(path), int(config), out), "sdm_gx_gemm_kernel_attrs")
+    return {"regs": out[0], "local_bytes": out[1], "static_smem": out[2], "max_threads": out[3]}
+
+
+def num_configs(path: int) -> int:
+    return int(_lib.sdm_gx_gemm_num_configs(int(path)))
+
+
+def device_error(clear: bool = True) -> int:
+    """The device error word (synchronizes the device); 0 means no kernel gave up a bounded wait."""
+    w = ctypes.c_uint32(0)
+    rc = _lib.sdm_gx_device_error(ctypes.byref(w), int(bool(clear)))
+    if rc not in (0, CODE["SDM_GX_E_DEVICE_FAULT"]):
+        raise GxGemmError(rc, "sdm_gx_device_error")
+    return int(w.value)
+
+
+def launch_counts() -> dict:
+    out = (ctypes.c_int64 * 3)()
+    _lib.sdm_gx_launch_counts(out)
+    return {"step": out[0], "producer": out[1], "pdl": out[2]}
+
+
+def strerror(status: int) -> str:
+    return _lib.sdm_gx_strerror(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.sdm_gx_abi_version())

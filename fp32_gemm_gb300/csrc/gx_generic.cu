@@ -1,0 +1,199 @@
+// The generic kernel of the gx_gemm step update (any element strides, 4-byte alignment, any C <= 256 and hd), and
+// the synthetic producer kernel of the chained workload. sm_103a.
+//
+// Generic kernel: CTAs of 256 threads loop over tiles of TI rows x 64 columns of one chunk (grid <= resident slots).
+// Thread (tx, ty) of a 16 x 16 layout owns rows i0 + ty + 16 r (r < TI / 16) and columns c0 + tx + 16 q (q < 4), so
+// global reads and writes of d_u are coalesced along c. The j range is staged KB = 32 rows at a time into shared
+// memory (xs[KB][TI] from x[n, j, i], ds[KB][64] from d_dv[n, j, c], zero past C / hd) with plain loads, and every
+// output runs the chain acc = fmaf(x[n,j,i], d_dv[n,j,c], acc), j = 0..C-1 in order from +0, then d_u + acc
+// (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring formula and gx_gemm_kernel).
+// Programmatic dependent launch: the first tile's d_u values are read into registers before griddepcontrol.wait;
+// x, d_dv are read and d_u written after it.
+#include "gx_device.cuh"
+#include "gx_internal.h"
+
+namespace sdmgx {
+namespace {
+
+constexpr int kGenTC = 64, kGenKB = 32, kGenNT = 256, kGenTX = 16, kGenTY = 16, kGenRC = kGenTC / kGenTX;
+
+template <int TI>
+__global__ void __launch_bounds__(kGenNT) gx_generic_kernel(const GenericParams p) {
+    constexpr int RI = TI / kGenTY;
+    __shared__ float xs[kGenKB][TI];
+    __shared__ float ds[kGenKB][kGenTC];
+    const int tx = static_cast<int>(threadIdx.x) % kGenTX;
+    const int ty = static_cast<int>(threadIdx.x) / kGenTX;
+    const int per_chunk = p.nib * p.ncb;
+    bool waited = false;
+    for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x)) {
+        const int pp = t / per_chunk;
+        const int rem = t - pp * per_chunk;
+        const int ib = rem / p.ncb;
+        const int cb = rem - ib * p.ncb;
+        const int64_t n = p.n_base + pp;
+        const int i0 = ib * TI, c0 = cb * kGenTC;
+        const float *xn = p.x + n * p.x_sn;
+        const float *dvn = p.dv + n * p.dv_sn;
+        float *dun = p.du + n * p.du_sn;
+        float u[RI][kGenRC];
+#pragma unroll
+        for (int r = 0; r < RI; ++r) {
+            const int i = i0 + ty + kGenTY * r;
+#pragma unroll
+            for (int q = 0; q < kGenRC; ++q) {
+                const int c = c0 + tx + kGenTX * q;
+                u[r][q] = (i < p.C && c < p.hd) ? dun[static_cast<int64_t>(i) * p.du_si + c] : 0.0f;
+            }
+        }
+        if (!waited) {
+            dev::grid_dependency_wait();
+            dev::launch_dependents();
+            waited = true;
+        }
+        float acc[RI][kGenRC];
+#pragma unroll
+        for (int r = 0; r < RI; ++r) {
+#pragma unroll
+            for (int q = 0; q < kGenRC; ++q) acc[r][q] = 0.0f;
+        }
+        for (int j0 = 0; j0 < p.C; j0 += kGenKB) {
+            const int nj = (p.C - j0) < kGenKB ? (p.C - j0) : kGenKB;
+            __syncthreads();   // the previous block's reads are done before the buffers are overwritten
+            for (int e = static_cast<int>(threadIdx.x); e < kGenKB * TI; e += kGenNT) {
+                const int jj = e / TI, ii = e - jj * TI;
+                xs[jj][ii] = (jj < nj && i0 + ii < p.C) ? xn[static_cast<int64_t>(j0 + jj) * p.x_sj + i0 + ii] : 0.0f;
+            }
+            for (int e = static_cast<int>(threadIdx.x); e < kGenKB * kGenTC; e += kGenNT) {
+                const int jj = e / kGenTC, cc = e - jj * kGenTC;
+                ds[jj][cc] =
+                    (jj < nj && c0 + cc < p.hd) ? dvn[static_cast<int64_t>(j0 + jj) * p.dv_sj + c0 + cc] : 0.0f;
+            }
+            __syncthreads();
+            for (int jj = 0; jj < nj; ++jj) {
+                float d[kGenRC];
+#pragma unroll
+                for (int q = 0; q < kGenRC; ++q) d[q] = ds[jj][tx + kGenTX * q];
+#pragma unroll
+                for (int r = 0; r < RI; ++r) {
+                    const float xv = xs[jj][ty + kGenTY * r];
+#pragma unroll
+                    for (int q = 0; q < kGenRC; ++q) acc[r][q] = fmaf(xv, d[q], acc[r][q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RI; ++r) {
+            const int i = i0 + ty + kGenTY * r;
+            if (i >= p.C) continue;
+#pragma unroll
+            for (int q = 0; q < kGenRC; ++q) {
+                const int c = c0 + tx + kGenTX * q;
+                if (c < p.hd) dun[static_cast<int64_t>(i) * p.du_si + c] = __fadd_rn(u[r][q], acc[r][q]);
+            }
+        }
+    }
+    if (!waited) {   // a CTA without a tile still orders itself after the predecessor
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+    }
+}
+
+template <int TI>
+cudaError_t launch_generic(const GenericParams &p, int grid, cudaStream_t st, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kGenNT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gx_generic_kernel<TI>, p);
+}
+
+template <int TI>
+ConfigInfo generic_info() {
+    return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32};
+}
+
+struct GEntry {
+    ConfigInfo info;
+    const void *fn;
+    cudaError_t (*launch)(const GenericParams &, int, cudaStream_t, int);
+};
+const GEntry kGen[] = {
+    {generic_info<16>(), reinterpret_cast<const void *>(&gx_generic_kernel<16>), &launch_generic<16>},
+    {generic_info<32>(), reinterpret_cast<const void *>(&gx_generic_kernel<32>), &launch_generic<32>},
+    {generic_info<64>(), reinterpret_cast<const void *>(&gx_generic_kernel<64>), &launch_generic<64>},
+};
+
+// ---- synthetic producer: d_dv[base + e] = +-S[base + e], e < count --------------------------------------------------
+// The first grid-wide pass of S is read before griddepcontrol.wait; every write of d_dv comes after it.
+constexpr int kProdNT = 256;
+
+__global__ void __launch_bounds__(kProdNT) gx_producer_kernel(float *__restrict__ dv, const float *__restrict__ S,
+                                                               int64_t base, int64_t count, uint32_t flip, int vec) {
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * kProdNT;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * kProdNT + threadIdx.x;
+    if (vec) {
+        const float4 *src = reinterpret_cast<const float4 *>(S + base);
+        float4 *dst = reinterpret_cast<float4 *>(dv + base);
+        const int64_t nv = count / 4;
+        float4 v = tid < nv ? src[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+        for (int64_t e = tid; e < nv; e += nthr) {
+            if (e != tid) v = src[e];
+            uint4 b = *reinterpret_cast<uint4 *>(&v);
+            b.x ^= flip;
+            b.y ^= flip;
+            b.z ^= flip;
+            b.w ^= flip;
+            dst[e] = *reinterpret_cast<float4 *>(&b);
+        }
+    } else {
+        float v = tid < count ? S[base + tid] : 0.0f;
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+        for (int64_t e = tid; e < count; e += nthr) {
+            if (e != tid) v = S[base + e];
+            dv[base + e] = __uint_as_float(__float_as_uint(v) ^ flip);
+        }
+    }
+}
+
+}  // namespace
+
+int generic_num_configs() { return static_cast<int>(sizeof(kGen) / sizeof(kGen[0])); }
+const ConfigInfo &generic_config(int k) { return kGen[k].info; }
+const void *generic_kernel(int k) { return kGen[k].fn; }
+cudaError_t generic_launch(int k, const GenericParams &p, int grid, cudaStream_t st, int pdl) {
+    return kGen[k].launch(p, grid, st, pdl);
+}
+
+cudaError_t producer_launch(float *dv, const float *S, int64_t base, int64_t count, int negate, cudaStream_t st,
+                            int pdl, int sms) {
+    if (count <= 0) return cudaSuccess;
+    const int vec = ((reinterpret_cast<uintptr_t>(dv + base) | reinterpret_cast<uintptr_t>(S + base)) & 15u) == 0 &&
+                    (count % 4) == 0;
+    const int64_t units = vec ? count / 4 : count;
+    int64_t blocks = (units + kProdNT - 1) / kProdNT;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kProdNT);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gx_producer_kernel, dv, S, base, count, negate ? 0x80000000u : 0u, vec);
+}
+
+}  // namespace sdmgx

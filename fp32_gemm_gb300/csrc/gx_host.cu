@@ -1,0 +1,638 @@
+// Host side of the gx_gemm C ABI: argument validation, per-device state, tile-configuration choice (the plan
+// cache's geometry rule), TMA descriptor encoding, plans and the multi-step driver.
+//
+// Follows the page's launcher and plan entry points (sparse_delta_memory/cuda/gx_gemm_cuda.py: gx_gemm's checks,
+// set_smem, gx_gemm_plan / gx_gemm_plan_launch, make_step), re-designed as a C ABI: every argument check runs before
+// any CUDA call and returns a status code instead of throwing; a plan is a host struct holding the validated
+// pointers, the geometry and the encoded tensor maps, and a launch patches only the step's chunk offset.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gx_internal.h"
+#include "sdm_gx_gemm.h"
+
+// The device error word: bits of sdmgx::kErr* set by kernels whose bounded waits expired. One word per device (each
+// device's module instance has its own copy); its device address is looked up once per device.
+__device__ uint32_t g_sdm_gx_error_word;
+
+namespace {
+
+using namespace sdmgx;
+
+constexpr int64_t kTwo31 = int64_t(1) << 31;
+constexpr int64_t kMaxSpanElems = int64_t(1) << 60;
+constexpr int64_t kMaxStride = int64_t(1) << 40;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxConfigs = 32;
+constexpr int64_t kWaitTimeoutNs = 2000000000LL;   // 2 s: a healthy wait lasts microseconds
+constexpr uint64_t kPlanMagic = 0x31504d4547584753ull;   // "SGXGEMP1"
+
+thread_local int t_last_cuda = 0;
+std::atomic<int64_t> g_count_step{0}, g_count_producer{0}, g_count_pdl{0};
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda = static_cast<int>(e);
+    return SDM_GX_E_CUDA;
+}
+
+struct DevState {
+    bool init = false;
+    int status = 0;
+    int sms = 0, optin = 0, smem_per_sm = 0, major = 0, minor = 0;
+    uint32_t *err = nullptr;
+    int tma_occ[kMaxConfigs] = {};
+    int gen_occ[kMaxConfigs] = {};
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device setup, once (under the lock): attributes, the error word's address, every kernel's shared-memory
+// attribute and occupancy. Returns a status; *out points at the device's state.
+int device_state(int *dev_out, const DevState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return SDM_GX_E_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState &d = g_dev[dev];
+    if (!d.init) {
+        DevState n;
+        if ((e = cudaDeviceGetAttribute(&n.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&n.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&n.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&n.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&n.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return fail_cuda(e);
+        if (n.major != 10 || n.minor != 3) {
+            n.status = SDM_GX_E_UNSUPPORTED;
+            n.init = true;
+            d = n;
+            *dev_out = dev;
+            *out = &d;
+            return d.status;
+        }
+        if ((e = cudaGetSymbolAddress(reinterpret_cast<void **>(&n.err), g_sdm_gx_error_word)) != cudaSuccess)
+            return fail_cuda(e);
+        for (int k = 0; k < tma_num_configs() && k < kMaxConfigs; ++k) {
+            const ConfigInfo &ci = tma_config(k);
+            if (ci.smem > n.optin) continue;
+            if ((e = cudaFuncSetAttribute(tma_kernel(k), cudaFuncAttributeMaxDynamicSharedMemorySize, ci.smem)) !=
+                cudaSuccess)
+                return fail_cuda(e);
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n.tma_occ[k], tma_kernel(k), ci.threads,
+                                                                   ci.smem)) != cudaSuccess)
+                return fail_cuda(e);
+        }
+        for (int k = 0; k < generic_num_configs() && k < kMaxConfigs; ++k) {
+            const ConfigInfo &ci = generic_config(k);
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n.gen_occ[k], generic_kernel(k), ci.threads,
+                                                                   0)) != cudaSuccess)
+                return fail_cuda(e);
+        }
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q{};
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return fail_cuda(e != cudaSuccess ? e : cudaErrorNotSupported);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        n.init = true;
+        d = n;
+    }
+    *dev_out = dev;
+    *out = &d;
+    return d.status;
+}
+
+// ---- validation -------------------------------------------------------------------------------------------------
+struct Shape {
+    int64_t N;        // chunks the operands hold (for _step: (ti + 1) * P, the minimum)
+    int64_t P, C, hd;
+    sdm_gx_strides s;
+};
+
+bool layout_ok(int64_t rows, int64_t cols, int64_t sr, int64_t sn, int64_t N) {
+    if (sr < cols || sr > kMaxStride) return false;
+    if (sn < rows * sr || sn > kMaxSpanElems / N) return false;
+    return true;
+}
+
+struct Span {
+    uintptr_t lo, hi;
+};
+Span span_of(const float *p, int64_t n0, int64_t n1, int64_t sn, int64_t sr, int64_t rows, int64_t cols) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+    return Span{b + static_cast<uintptr_t>(n0 * sn) * 4u,
+                b + static_cast<uintptr_t>((n1 - 1) * sn + (rows - 1) * sr + cols) * 4u};
+}
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Checks shared by every entry point (before any CUDA call). n0 .. n1 - 1: the chunks whose spans must not overlap.
+int validate(const float *du, const float *x, const float *dv, const Shape &sh, int64_t n0, int64_t n1) {
+    if (du == nullptr || x == nullptr || dv == nullptr) return SDM_GX_E_NULL;
+    if (sh.C < 1 || sh.C > 256 || sh.hd < 1 || sh.hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    const sdm_gx_strides &s = sh.s;
+    if (!layout_ok(sh.C, sh.C, s.x_sj, s.x_sn, sh.N) || !layout_ok(sh.C, sh.hd, s.dv_sj, s.dv_sn, sh.N) ||
+        !layout_ok(sh.C, sh.hd, s.du_si, s.du_sn, sh.N))
+        return SDM_GX_E_STRIDE;
+    if ((reinterpret_cast<uintptr_t>(du) | reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(dv)) & 3u)
+        return SDM_GX_E_ALIGN;
+    const Span su = span_of(du, n0, n1, s.du_sn, s.du_si, sh.C, sh.hd);
+    const Span sx = span_of(x, n0, n1, s.x_sn, s.x_sj, sh.C, sh.C);
+    const Span sv = span_of(dv, n0, n1, s.dv_sn, s.dv_sj, sh.C, sh.hd);
+    if (overlaps(su, sx) || overlaps(su, sv)) return SDM_GX_E_OVERLAP;
+    return SDM_GX_OK;
+}
+
+sdm_gx_strides contiguous(int64_t C, int64_t hd) {
+    sdm_gx_strides s;
+    s.x_sn = C * C;
+    s.x_sj = C;
+    s.dv_sn = C * hd;
+    s.dv_sj = hd;
+    s.du_sn = C * hd;
+    s.du_si = hd;
+    return s;
+}
+
+bool tma_eligible(const float *du, const float *x, const float *dv, const sdm_gx_strides &s) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(du) | reinterpret_cast<uintptr_t>(x) |
+                        reinterpret_cast<uintptr_t>(dv);
+    if (a & 15u) return false;
+    const int64_t st = s.x_sn | s.x_sj | s.dv_sn | s.dv_sj | s.du_sn | s.du_si;
+    if (st & 3) return false;
+    // tensor-map strides are in bytes and must stay below 2^40
+    const int64_t mx = std::max({s.x_sn, s.x_sj, s.dv_sn, s.dv_sj, s.du_sn, s.du_si});
+    return mx * 4 < kMaxStride;
+}
+
+// ---- the launch description ----------------------------------------------------------------------------------------
+struct Launch {
+    int path = 0, config = 0, grid = 0, device = 0;
+    int64_t n_first = 0;   // chunk index of the tensor maps' / pointers' origin
+    int32_t P = 0;
+    TmaParams tma;
+    GenericParams gen;
+    sdm_gx_geom geom;
+};
+
+double fma_share(const ConfigInfo &ci) {
+    const int sr = std::max(1, ci.RM / 4), sn = std::max(1, ci.RN / 4);
+    return static_cast<double>(ci.RM * ci.RN) / (ci.RM * ci.RN + sr + sn);
+}
+
+// The geometry rule (our re-derivation of the page's one-wave rows rule for this kernel family): estimate the
+// step time of every tile configuration from the busiest SM's padded FMA work, the FMA share of its inner loop and
+// the number of consumer warps per SM sub-partition, plus a per-tile latency term; take the fastest.
+int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
+    if (forced >= 0) return forced;
+    double best = 1e300;
+    int bk = -1;
+    for (int k = 0; k < tma_num_configs(); ++k) {
+        const ConfigInfo &ci = tma_config(k);
+        const int occ = d.tma_occ[k];
+        if (occ < 1) continue;
+        const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+        if (tiles >= kTwo31) continue;
+        const int64_t per_sm = (tiles + d.sms - 1) / d.sms;
+        const int64_t slots = static_cast<int64_t>(d.sms) * occ;
+        const int64_t per_cta = (tiles + slots - 1) / slots;
+        const double warps = static_cast<double>(std::min<int64_t>(occ, per_sm) * ci.consumer_warps);
+        const double rate = 128.0 * fma_share(ci) * std::min(1.0, warps / 4.0);
+        const double work = static_cast<double>(per_sm) * ci.TI * ci.TC * C;
+        const double lat = static_cast<double>(per_cta) * (4.0 * C + 600.0) + 2500.0;
+        const double est = work / rate + lat;
+        if (est < best * 0.999) {
+            best = est;
+            bk = k;
+        }
+    }
+    return bk;
+}
+
+int choose_generic_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
+    if (forced >= 0) return forced;
+    for (int k = 0; k < generic_num_configs(); ++k) {
+        const ConfigInfo &ci = generic_config(k);
+        const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+        if (tiles <= static_cast<int64_t>(d.sms) * std::max(1, d.gen_occ[k])) return k;
+    }
+    return generic_num_configs() - 1;
+}
+
+CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t rows, int64_t chunks, int64_t sr,
+                    int64_t sn, int box_inner, int box_rows) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(chunks)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(sr) * 4u, static_cast<cuuint64_t>(sn) * 4u};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// Build the launch description for chunks n_first .. n_first + n_count - 1 (pointers and tensor maps originate at
+// n_first). Runs after validate(); makes CUDA calls (device state, descriptor encoding).
+int build_launch(float *du, const float *x, const float *dv, const Shape &sh, int64_t n_first, int64_t n_count,
+                 unsigned flags, Launch *L) {
+    const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
+                           SDM_GX_FLAG_CTAS_MASK;
+    if (flags & ~known) return SDM_GX_E_FLAGS;
+    int dev = 0;
+    const DevState *dsp = nullptr;
+    int rc = device_state(&dev, &dsp);
+    if (rc != SDM_GX_OK) return rc;
+    const DevState &d = *dsp;
+    // operands must be device memory of this device
+    const void *ptrs[3] = {du, x, dv};
+    for (const void *q : ptrs) {
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, q);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SDM_GX_E_DEVICE;
+        }
+        if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != dev)
+            return SDM_GX_E_DEVICE;
+    }
+    const sdm_gx_strides &s = sh.s;
+    const int forced = static_cast<int>(flags & SDM_GX_FLAG_CONFIG_MASK) - 1;
+    const int forced_occ = static_cast<int>((flags & SDM_GX_FLAG_CTAS_MASK) >> SDM_GX_FLAG_CTAS_SHIFT);
+    const bool use_tma = !(flags & SDM_GX_FLAG_GENERIC) && tma_eligible(du, x, dv, s);
+    Launch l;
+    l.device = dev;
+    l.n_first = n_first;
+    l.P = static_cast<int32_t>(sh.P);
+    float *du0 = du + n_first * s.du_sn;
+    const float *x0 = x + n_first * s.x_sn;
+    const float *dv0 = dv + n_first * s.dv_sn;
+    const ConfigInfo *ci = nullptr;
+    int occ = 0;
+    if (use_tma) {
+        if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
+        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced);
+        if (k < 0) return SDM_GX_E_SMEM;
+        ci = &tma_config(k);
+        if (ci->smem > d.optin || d.tma_occ[k] < 1) return SDM_GX_E_SMEM;
+        occ = d.tma_occ[k];
+        l.path = 1;
+        l.config = k;
+        TmaParams &t = l.tma;
+        std::memset(&t, 0, sizeof(t));
+        CUresult r;
+        if ((r = encode_map(&t.tm_x, x0, sh.C, sh.C, n_count, s.x_sj, s.x_sn, ci->TI, ci->KB)) != CUDA_SUCCESS ||
+            (r = encode_map(&t.tm_dv, dv0, sh.hd, sh.C, n_count, s.dv_sj, s.dv_sn, ci->TC, ci->KB)) !=
+                CUDA_SUCCESS ||
+            (r = encode_map(&t.tm_du, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, ci->TI)) != CUDA_SUCCESS)
+            return fail_cuda(r == CUDA_ERROR_INVALID_VALUE ? cudaErrorInvalidValue : cudaErrorUnknown);
+        t.du = du0;
+        t.du_sn = s.du_sn;
+        t.du_si = s.du_si;
+        t.P = static_cast<int32_t>(sh.P);
+        t.C = static_cast<int32_t>(sh.C);
+        t.hd = static_cast<int32_t>(sh.hd);
+        t.nib = static_cast<int32_t>((sh.C + ci->TI - 1) / ci->TI);
+        t.ncb = static_cast<int32_t>((sh.hd + ci->TC - 1) / ci->TC);
+        const int64_t tiles = sh.P * t.nib * t.ncb;
+        if (tiles >= kTwo31) return SDM_GX_E_GRID;
+        t.ntiles = static_cast<int32_t>(tiles);
+        t.prefetch = (flags & SDM_GX_FLAG_NO_PREFETCH) ? 0 : 1;
+        t.timeout_ns = kWaitTimeoutNs;
+        t.err = d.err;
+    } else {
+        if (forced >= generic_num_configs()) return SDM_GX_E_FLAGS;
+        const int k = choose_generic_config(d, sh.P, sh.C, sh.hd, forced);
+        ci = &generic_config(k);
+        occ = std::max(1, d.gen_occ[k]);
+        l.path = 0;
+        l.config = k;
+        GenericParams &g = l.gen;
+        g.du = du0;
+        g.x = x0;
+        g.dv = dv0;
+        g.x_sn = s.x_sn;
+        g.x_sj = s.x_sj;
+        g.dv_sn = s.dv_sn;
+        g.dv_sj = s.dv_sj;
+        g.du_sn = s.du_sn;
+        g.du_si = s.du_si;
+        g.P = static_cast<int32_t>(sh.P);
+        g.C = static_cast<int32_t>(sh.C);
+        g.hd = static_cast<int32_t>(sh.hd);
+        g.nib = static_cast<int32_t>((sh.C + ci->TI - 1) / ci->TI);
+        g.ncb = static_cast<int32_t>((sh.hd + ci->TC - 1) / ci->TC);
+        const int64_t tiles = sh.P * g.nib * g.ncb;
+        if (tiles >= kTwo31) return SDM_GX_E_GRID;
+        g.ntiles = static_cast<int32_t>(tiles);
+    }
+    if (forced_occ > 0) occ = std::min(occ, forced_occ);
+    const int64_t tiles = l.path ? l.tma.ntiles : l.gen.ntiles;
+    const int64_t slots = static_cast<int64_t>(d.sms) * occ;
+    l.grid = static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
+    sdm_gx_geom &gm = l.geom;
+    gm.path = l.path;
+    gm.config = l.config;
+    gm.TI = ci->TI;
+    gm.TC = ci->TC;
+    gm.KB = ci->KB;
+    gm.stages = ci->stages;
+    gm.threads = ci->threads;
+    gm.smem_bytes = ci->smem;
+    gm.tiles = tiles;
+    gm.ctas = l.grid;
+    gm.ctas_per_sm = occ;
+    gm.sms = d.sms;
+    gm.one_wave = tiles <= slots ? 1 : 0;
+    *L = l;
+    return SDM_GX_OK;
+}
+
+int launch(const Launch &l, int64_t ti, cudaStream_t st, int pdl) {
+    const int64_t nb = ti * l.P - l.n_first;
+    cudaError_t e;
+    if (l.path == 1) {
+        TmaParams p = l.tma;
+        p.n_base = static_cast<int32_t>(nb);
+        e = tma_launch(l.config, p, l.grid, st, pdl);
+    } else {
+        GenericParams p = l.gen;
+        p.n_base = nb;
+        e = generic_launch(l.config, p, l.grid, st, pdl);
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    g_count_step.fetch_add(1, std::memory_order_relaxed);
+    if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+    return SDM_GX_OK;
+}
+
+}  // namespace
+
+// ======================================================= plans =======================================================
+struct sdm_gx_plan {
+    uint64_t magic;
+    const sdm_gx_plan *self;
+    int64_t N, P, C, hd, ti_max;
+    Shape shape;
+    float *du;
+    const float *x;
+    const float *dv;
+    Launch launch;
+};
+
+namespace {
+int plan_check(const sdm_gx_plan *pl) {
+    if (pl == nullptr || pl->magic != kPlanMagic || pl->self != pl) return SDM_GX_E_PLAN;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev != pl->launch.device) return SDM_GX_E_PLAN_DEVICE;
+    return SDM_GX_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int sdm_gx_abi_version(void) { return SDM_GX_ABI_VERSION; }
+
+int sdm_gx_gemm_step(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t P, int64_t C, int64_t hd,
+                     cudaStream_t stream, int pdl) {
+    if (d_u == nullptr || x == nullptr || d_dv == nullptr) return SDM_GX_E_NULL;
+    if (C < 1 || C > 256 || hd < 1 || hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    if (P < 1 || P >= kTwo31 || ti < 0 || ti > (kTwo31 - 1) / P - 1) return SDM_GX_E_RANGE;
+    Shape sh{(ti + 1) * P, P, C, hd, contiguous(C, hd)};
+    int rc = validate(d_u, x, d_dv, sh, ti * P, (ti + 1) * P);
+    if (rc != SDM_GX_OK) return rc;
+    Launch l;
+    rc = build_launch(d_u, x, d_dv, sh, ti * P, P, 0u, &l);
+    if (rc != SDM_GX_OK) return rc;
+    return launch(l, ti, stream, pdl);
+}
+
+static int ex_common(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t N, int64_t P, int64_t C,
+                     int64_t hd, const sdm_gx_strides *strides, Shape *sh) {
+    if (d_u == nullptr || x == nullptr || d_dv == nullptr) return SDM_GX_E_NULL;
+    if (C < 1 || C > 256 || hd < 1 || hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    if (N < 1 || N >= kTwo31 || P < 1 || P > N || ti < 0 || ti >= N / P) return SDM_GX_E_RANGE;
+    *sh = Shape{N, P, C, hd, strides ? *strides : contiguous(C, hd)};
+    return validate(d_u, x, d_dv, *sh, 0, N);
+}
+
+int sdm_gx_gemm_step_ex(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t N, int64_t P, int64_t C,
+                        int64_t hd, const sdm_gx_strides *strides, cudaStream_t stream, int pdl, unsigned flags) {
+    Shape sh;
+    int rc = ex_common(d_u, x, d_dv, ti, N, P, C, hd, strides, &sh);
+    if (rc != SDM_GX_OK) return rc;
+    Launch l;
+    rc = build_launch(d_u, x, d_dv, sh, ti * P, P, flags, &l);
+    if (rc != SDM_GX_OK) return rc;
+    return launch(l, ti, stream, pdl);
+}
+
+int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C,
+                         int64_t hd, const sdm_gx_strides *strides, unsigned flags, sdm_gx_geom *out) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    Shape sh;
+    int rc = ex_common(const_cast<float *>(d_u), x, d_dv, 0, N, P, C, hd, strides, &sh);
+    if (rc != SDM_GX_OK) return rc;
+    Launch l;
+    rc = build_launch(const_cast<float *>(d_u), x, d_dv, sh, 0, N, flags, &l);
+    if (rc != SDM_GX_OK) return rc;
+    *out = l.geom;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
+                            int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max, unsigned flags) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    *out = nullptr;
+    Shape sh;
+    int rc = ex_common(d_u, x, d_dv, ti_max, N, P, C, hd, strides, &sh);
+    if (rc != SDM_GX_OK) return rc;
+    Launch l;
+    rc = build_launch(d_u, x, d_dv, sh, 0, N, flags, &l);
+    if (rc != SDM_GX_OK) return rc;
+    sdm_gx_plan *pl = static_cast<sdm_gx_plan *>(std::malloc(sizeof(sdm_gx_plan)));
+    if (pl == nullptr) return SDM_GX_E_ALLOC;
+    std::memset(static_cast<void *>(pl), 0, sizeof(*pl));
+    pl->magic = kPlanMagic;
+    pl->self = pl;
+    pl->N = N;
+    pl->P = P;
+    pl->C = C;
+    pl->hd = hd;
+    pl->ti_max = ti_max;
+    pl->shape = sh;
+    pl->du = d_u;
+    pl->x = x;
+    pl->dv = d_dv;
+    pl->launch = l;
+    *out = pl;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    if (ti < 0 || ti > plan->ti_max) return SDM_GX_E_PLAN_TI;
+    return launch(plan->launch, ti, stream, pdl);
+}
+
+int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, int64_t ti_end, cudaStream_t stream, int pdl) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    const int64_t step = ti_begin <= ti_end ? 1 : -1;
+    const int64_t lo = step > 0 ? ti_begin : ti_end + 1;
+    const int64_t hi = step > 0 ? ti_end - 1 : ti_begin;
+    if (ti_begin != ti_end && (lo < 0 || hi > plan->ti_max)) return SDM_GX_E_PLAN_TI;
+    for (int64_t ti = ti_begin; ti != ti_end; ti += step) {
+        rc = launch(plan->launch, ti, stream, pdl);
+        if (rc != SDM_GX_OK) return rc;
+    }
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64_t ti_begin, int64_t ti_end,
+                                  cudaStream_t stream, int pdl) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    if (S == nullptr) return SDM_GX_E_NULL;
+    if (reinterpret_cast<uintptr_t>(S) & 3u) return SDM_GX_E_ALIGN;
+    const Shape &sh = plan->shape;
+    if (sh.s.dv_sj != sh.hd || sh.s.dv_sn != sh.C * sh.hd) return SDM_GX_E_STRIDE;   // the producer is contiguous
+    const Span ss = span_of(S, 0, sh.N, sh.s.dv_sn, sh.s.dv_sj, sh.C, sh.hd);
+    const Span sv = span_of(plan->dv, 0, sh.N, sh.s.dv_sn, sh.s.dv_sj, sh.C, sh.hd);
+    const Span su = span_of(plan->du, 0, sh.N, sh.s.du_sn, sh.s.du_si, sh.C, sh.hd);
+    if (overlaps(ss, sv) || overlaps(ss, su)) return SDM_GX_E_OVERLAP;
+    const int64_t step = ti_begin <= ti_end ? 1 : -1;
+    const int64_t lo = step > 0 ? ti_begin : ti_end + 1;
+    const int64_t hi = step > 0 ? ti_end - 1 : ti_begin;
+    if (ti_begin != ti_end && (lo < 0 || hi > plan->ti_max)) return SDM_GX_E_PLAN_TI;
+    const int64_t per_step = sh.P * sh.C * sh.hd;
+    const int sms = g_dev[plan->launch.device].sms;
+    for (int64_t ti = ti_begin; ti != ti_end; ti += step) {
+        cudaError_t e = producer_launch(const_cast<float *>(plan->dv), S,
+                                        ti * per_step, per_step, static_cast<int>(ti & 1), stream, pdl, sms);
+        if (e != cudaSuccess) return fail_cuda(e);
+        g_count_producer.fetch_add(1, std::memory_order_relaxed);
+        if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+        rc = launch(plan->launch, ti, stream, pdl);
+        if (rc != SDM_GX_OK) return rc;
+    }
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    if (plan == nullptr || plan->magic != kPlanMagic || plan->self != plan) return SDM_GX_E_PLAN;
+    *out = plan->launch.geom;
+    return SDM_GX_OK;
+}
+
+void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan) {
+    if (plan == nullptr || plan->magic != kPlanMagic || plan->self != plan) return;
+    plan->magic = 0;
+    plan->self = nullptr;
+    std::free(plan);
+}
+
+int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int64_t P, int64_t C, int64_t hd,
+                         cudaStream_t stream, int pdl) {
+    if (d_dv == nullptr || S == nullptr) return SDM_GX_E_NULL;
+    if (C < 1 || C > 256 || hd < 1 || hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    if (P < 1 || P >= kTwo31 || ti < 0 || ti > (kTwo31 - 1) / P - 1) return SDM_GX_E_RANGE;
+    if ((reinterpret_cast<uintptr_t>(d_dv) | reinterpret_cast<uintptr_t>(S)) & 3u) return SDM_GX_E_ALIGN;
+    const int64_t per_step = P * C * hd;
+    const Span a = span_of(d_dv, ti * P, (ti + 1) * P, C * hd, hd, C, hd);
+    const Span b = span_of(S, ti * P, (ti + 1) * P, C * hd, hd, C, hd);
+    if (overlaps(a, b)) return SDM_GX_E_OVERLAP;
+    int dev = 0;
+    const DevState *d = nullptr;
+    int rc = device_state(&dev, &d);
+    if (rc != SDM_GX_OK) return rc;
+    cudaError_t e = producer_launch(d_dv, S, ti * per_step, per_step, static_cast<int>(ti & 1), stream, pdl, d->sms);
+    if (e != cudaSuccess) return fail_cuda(e);
+    g_count_producer.fetch_add(1, std::memory_order_relaxed);
+    if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    const void *fn = nullptr;
+    if (path == 1 && config >= 0 && config < tma_num_configs()) fn = tma_kernel(config);
+    if (path == 0 && config >= 0 && config < generic_num_configs()) fn = generic_kernel(config);
+    if (fn == nullptr) return SDM_GX_E_FLAGS;
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, fn);
+    if (e != cudaSuccess) return fail_cuda(e);
+    out[0] = a.numRegs;
+    out[1] = static_cast<int64_t>(a.localSizeBytes);
+    out[2] = static_cast<int64_t>(a.sharedSizeBytes);
+    out[3] = a.maxThreadsPerBlock;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_num_configs(int32_t path) {
+    if (path == 1) return tma_num_configs();
+    if (path == 0) return generic_num_configs();
+    return 0;
+}
+
+int sdm_gx_device_error(uint32_t *word, int clear) {
+    if (word == nullptr) return SDM_GX_E_NULL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e);
+    uint32_t w = 0;
+    if ((e = cudaMemcpyFromSymbol(&w, g_sdm_gx_error_word, sizeof(w))) != cudaSuccess) return fail_cuda(e);
+    *word = w;
+    if (clear) {
+        const uint32_t z = 0;
+        if ((e = cudaMemcpyToSymbol(g_sdm_gx_error_word, &z, sizeof(z))) != cudaSuccess) return fail_cuda(e);
+    }
+    return w ? SDM_GX_E_DEVICE_FAULT : SDM_GX_OK;
+}
+
+void sdm_gx_launch_counts(int64_t out[3]) {
+    if (out == nullptr) return;
+    out[0] = g_count_step.load();
+    out[1] = g_count_producer.load();
+    out[2] = g_count_pdl.load();
+}
+
+int sdm_gx_last_cuda_error(void) { return t_last_cuda; }
+
+const char *sdm_gx_strerror(int status) {
+    switch (status) {
+        case SDM_GX_OK: return "ok";
+        case SDM_GX_E_NULL: return "a required pointer is NULL";
+        case SDM_GX_E_SHAPE: return "need 1 <= C <= 256 and 1 <= hd < 2^20";
+        case SDM_GX_E_RANGE: return "step out of range (need 1 <= P <= N < 2^31 and 0 <= ti < N / P)";
+        case SDM_GX_E_ALIGN: return "operands must be 4-byte aligned";
+        case SDM_GX_E_OVERLAP: return "d_u overlaps x or d_dv (the in-place update needs disjoint operands)";
+        case SDM_GX_E_STRIDE: return "strides do not describe a non-overlapping [N, rows, cols] layout";
+        case SDM_GX_E_GRID: return "too many tiles in one step";
+        case SDM_GX_E_SMEM: return "shared memory exceeds the device's opt-in limit";
+        case SDM_GX_E_DEVICE: return "operands must be device memory of the current device";
+        case SDM_GX_E_PLAN: return "plan is NULL or corrupt";
+        case SDM_GX_E_PLAN_TI: return "step outside [0, ti_max] of the plan";
+        case SDM_GX_E_PLAN_DEVICE: return "the current device is not the plan's device";
+        case SDM_GX_E_FLAGS: return "unknown flags or invalid forced configuration";
+        case SDM_GX_E_CUDA: return "a CUDA runtime call failed (see sdm_gx_last_cuda_error)";
+        case SDM_GX_E_DEVICE_FAULT: return "a kernel gave up a bounded wait (device error word set)";
+        case SDM_GX_E_UNSUPPORTED: return "the current device is not an sm_103 GPU";
+        case SDM_GX_E_ALLOC: return "host allocation failed";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

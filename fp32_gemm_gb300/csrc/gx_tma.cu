@@ -1,0 +1,326 @@
+// The TMA-fed, warp-specialised FP32 kernel of the gx_gemm step update (sm_103a).
+//
+// What it computes (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring formula and gx_gemm_kernel): for every
+// chunk n of the step, row i < C and column c < hd, one thread runs acc = +0; acc = fmaf(x[n,j,i], d_dv[n,j,c], acc)
+// for j = 0..C-1 in order, then writes d_u[n,i,c] + acc (one rounding). Tensor cores are not used: their rounding
+// cannot reproduce that chain.
+//
+// How (our design for GB300, not the page's cp.async kernel):
+//   * Persistent CTAs (grid <= resident slots) loop over tiles of TI rows x TC columns of one chunk.
+//   * One producer warp (one elected lane) streams the operands with TMA (cp.async.bulk.tensor, 3-D tiled boxes of the
+//     whole tensors, hardware zero fill past C / hd) into a ring of ST shared-memory stages of KB j-rows each:
+//     xs[KB][TI] (x rows j, columns i) and ds[KB][TC] (d_dv rows j, columns c). mbarrier full/empty pairs with
+//     transaction counts hand stages between producer and consumers. The d_u tile [TI][TC] is staged the same way.
+//   * Consumer warps hold an RM x RN register tile per thread (4 x 8 lanes per warp, rows and columns in vectors of
+//     up to 4) and run the j-chain in order with fmaf: per j, RM/4 + RN/4 vector shared loads feed RM*RN FMAs.
+//   * Programmatic dependent launch: before griddepcontrol.wait the producer issues the first tile's d_u box and the
+//     x boxes of the first ST stages, and prefetches that tile's d_dv boxes into L2 (no visible effect: L2 is the
+//     point of coherence). d_dv is loaded into shared memory only after the wait; d_u is written only after it.
+//   * Every mbarrier wait is bounded (globaltimer); on expiry the thread sets a bit in the device error word and the
+//     CTA unwinds; the producer first waits (bounded) for the copies it issued.
+#include "gx_device.cuh"
+#include "gx_internal.h"
+
+namespace sdmgx {
+namespace {
+
+constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+template <int RM_, int RN_, int WM_, int WN_, int KB_, int ST_, int MINB_>
+struct TCfg {
+    static constexpr int RM = RM_, RN = RN_;       // per-thread tile: rows x columns
+    static constexpr int WM = WM_, WN = WN_;       // consumer warps along rows / columns
+    static constexpr int KB = KB_, ST = ST_;       // j rows per stage, stages
+    static constexpr int MINB = MINB_;             // CTAs per SM the register budget is sized for
+    static constexpr int LM = 4, LN = 8;           // lanes along rows / columns
+    static constexpr int VR = RM < 4 ? RM : 4, SR = RM / VR;
+    static constexpr int VN = RN < 4 ? RN : 4, SN = RN / VN;
+    static constexpr int TI = WM * RM * LM;
+    static constexpr int TC = WN * RN * LN;
+    static constexpr int NCW = WM * WN;
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int XS_BYTES = align_up(KB * TI * 4, 1024);
+    static constexpr int DS_BYTES = align_up(KB * TC * 4, 1024);
+    static constexpr int DU_BYTES = align_up(TI * TC * 4, 1024);
+    static constexpr int OFF_D = ST * XS_BYTES;
+    static constexpr int OFF_U = OFF_D + ST * DS_BYTES;
+    static constexpr int OFF_BAR = OFF_U + DU_BYTES;
+    static constexpr int NBAR = 2 * ST + 2;
+    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8, 128) + 1024;   // + slack for 1 KB alignment
+    static constexpr uint32_t STAGE_TX = static_cast<uint32_t>(KB * (TI + TC) * 4);
+    static constexpr uint32_t DU_TX = static_cast<uint32_t>(TI * TC * 4);
+    static constexpr int UNROLL = (RM * RN >= 64) ? 8 : ((RM * RN >= 16) ? 16 : 32);
+    static_assert(RM == 1 || RM == 2 || RM % 4 == 0, "RM: 1, 2 or a multiple of 4");
+    static_assert(RN == 1 || RN == 2 || RN % 4 == 0, "RN: 1, 2 or a multiple of 4");
+    static_assert(TI <= 256 && TC <= 256 && KB <= 256, "TMA box dimensions are at most 256");
+    static_assert(TI % 4 == 0 && TC % 4 == 0, "box rows must be multiples of 16 bytes");
+    static_assert(KB % UNROLL == 0 || UNROLL >= KB, "unroll divides KB");
+};
+
+struct Tile {
+    int32_t n, i0, c0;
+};
+
+template <class Cfg>
+__device__ __forceinline__ Tile decode_tile(const TmaParams &p, int t) {
+    const int per_chunk = p.nib * p.ncb;
+    const int pp = t / per_chunk;
+    const int rem = t - pp * per_chunk;
+    const int ib = rem / p.ncb;
+    const int cb = rem - ib * p.ncb;
+    return Tile{p.n_base + pp, ib * Cfg::TI, cb * Cfg::TC};
+}
+
+// The chain for nj consecutive j of one stage (j order preserved: jj ascending).
+template <class Cfg, bool FULL>
+__device__ __forceinline__ void chain_block(const float *__restrict__ xs, const float *__restrict__ ds,
+                                            const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                            float (&acc)[Cfg::RM][Cfg::RN], int nj) {
+    const int cnt = FULL ? Cfg::KB : nj;
+#pragma unroll(Cfg::UNROLL)
+    for (int jj = 0; jj < cnt; ++jj) {
+        float a[Cfg::RM], b[Cfg::RN];
+#pragma unroll
+        for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
+#pragma unroll
+        for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+#pragma unroll
+        for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+            for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+        }
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const __grid_constant__ TmaParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_s = dev::smem_addr(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    unsigned char *const base_g = smem_raw + (base_s - raw_s);
+    const uint32_t bar0 = base_s + Cfg::OFF_BAR;
+    const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
+    const uint32_t du_empty = du_full + 8u;
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::ST; ++s) {
+            dev::mbar_init(bar0 + 8u * s, 1);                       // full[s]: the producer's expect_tx arrive
+            dev::mbar_init(bar0 + 8u * (Cfg::ST + s), Cfg::NCW);    // empty[s]: one arrive per consumer warp
+        }
+        dev::mbar_init(du_full, 1);
+        dev::mbar_init(du_empty, Cfg::NCW);
+        dev::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int nk = (p.C + Cfg::KB - 1) / Cfg::KB;
+
+    if (warp == Cfg::NCW) {
+        // ------------------------------------------------ producer ------------------------------------------------
+        if (lane != 0) return;
+        int t = static_cast<int>(blockIdx.x);
+        int it = 0;          // stage iterations issued (over all tiles)
+        int du_issued = 0;   // d_u boxes issued
+        int npre = 0;        // stages of the first tile whose x box went out before the dependency wait
+        bool ok = true;
+        if (t < p.ntiles) {
+            dev::prefetch_tensormap(&p.tm_x);
+            dev::prefetch_tensormap(&p.tm_dv);
+            dev::prefetch_tensormap(&p.tm_du);
+            const Tile tl = decode_tile<Cfg>(p, t);
+            dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
+            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+            du_issued = 1;
+            npre = nk < Cfg::ST ? nk : Cfg::ST;
+            for (int s = 0; s < npre; ++s) {
+                dev::mbar_arrive_expect_tx(bar0 + 8u * s, Cfg::STAGE_TX);
+                dev::tma_load_3d(base_s + s * Cfg::XS_BYTES, &p.tm_x, tl.i0, s * Cfg::KB, tl.n, bar0 + 8u * s);
+            }
+            if (p.prefetch) {
+                for (int kb = 0; kb < nk; ++kb) dev::tma_prefetch_3d(&p.tm_dv, tl.c0, kb * Cfg::KB, tl.n);
+            }
+        }
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+        for (int tk = 0; t < p.ntiles && ok; t += static_cast<int>(gridDim.x), ++tk) {
+            const Tile tl = decode_tile<Cfg>(p, t);
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int s = it % Cfg::ST;
+                const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+                const uint32_t full = bar0 + 8u * s;
+                const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
+                if (it < npre) {   // armed, x already in flight: add the d_dv box
+                    dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, kb * Cfg::KB, tl.n, full);
+                    continue;
+                }
+                if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(full, Cfg::STAGE_TX);
+                dev::tma_load_3d(base_s + s * Cfg::XS_BYTES, &p.tm_x, tl.i0, kb * Cfg::KB, tl.n, full);
+                dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, kb * Cfg::KB, tl.n, full);
+            }
+            // The d_u box of this tile goes out after its k-blocks: the single d_u buffer is free once every consumer
+            // warp has finished the previous tile's epilogue, and the consumers need it only after this tile's last
+            // k-block. Issuing it here keeps the k-block stream running ahead across tile boundaries.
+            if (ok && tk > 0) {
+                if (!dev::mbar_wait(du_empty, static_cast<uint32_t>(tk - 1) & 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
+                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+                ++du_issued;
+            }
+        }
+        if (!ok) {
+            atomicOr(p.err, kErrProducerWait);
+            // Unwind: wait for the copies this thread issued (the last use of every stage, the last d_u box), so that
+            // no TMA write lands in shared memory after the CTA has exited. A failed wait can only happen at an
+            // iteration >= npre, so every stage armed before the dependency wait has received its d_dv box too and
+            // each drained phase does complete.
+            const int lo = it - Cfg::ST > 0 ? it - Cfg::ST : 0;
+            for (int k = lo; k < it; ++k) {
+                if (!dev::mbar_wait(bar0 + 8u * (k % Cfg::ST), static_cast<uint32_t>(k / Cfg::ST) & 1u, p.timeout_ns))
+                    atomicOr(p.err, kErrDrainWait);
+            }
+            if (du_issued > 0 && !dev::mbar_wait(du_full, static_cast<uint32_t>(du_issued - 1) & 1u, p.timeout_ns))
+                atomicOr(p.err, kErrDrainWait);
+        }
+        return;
+    }
+
+    // -------------------------------------------------- consumers --------------------------------------------------
+    const int wm = warp % Cfg::WM;
+    const int wn = warp / Cfg::WM;
+    const int lm = lane / Cfg::LN;
+    const int ln = lane % Cfg::LN;
+    int ro[Cfg::SR], co[Cfg::SN];
+#pragma unroll
+    for (int s = 0; s < Cfg::SR; ++s) ro[s] = wm * Cfg::RM * Cfg::LM + s * Cfg::VR * Cfg::LM + lm * Cfg::VR;
+#pragma unroll
+    for (int s = 0; s < Cfg::SN; ++s) co[s] = wn * Cfg::RN * Cfg::LN + s * Cfg::VN * Cfg::LN + ln * Cfg::VN;
+
+    dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
+    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U);
+    int it = 0;
+    int tk = 0;
+    for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x), ++tk) {
+        const Tile tl = decode_tile<Cfg>(p, t);
+        float acc[Cfg::RM][Cfg::RN];
+#pragma unroll
+        for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+            for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = 0.0f;   // +0: the chain's start value
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int s = it % Cfg::ST;
+            const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+            // warp-uniform decision: every lane leaves together or none does
+            if (!__all_sync(0xffffffffu, dev::mbar_wait(bar0 + 8u * s, ph, p.timeout_ns))) {
+                if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+                return;
+            }
+            const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
+            const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
+            const int nj = p.C - kb * Cfg::KB;
+            if (nj >= Cfg::KB) {
+                chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+            } else {
+                chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+        }
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(tk) & 1u, p.timeout_ns))) {
+            if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+            return;
+        }
+        // epilogue: d_u + acc, one rounding each, stored straight to global memory
+#pragma unroll
+        for (int sr = 0; sr < Cfg::SR; ++sr) {
+#pragma unroll
+            for (int er = 0; er < Cfg::VR; ++er) {
+                const int rl = ro[sr] + er;
+                const int i = tl.i0 + rl;
+                if (i >= p.C) continue;
+                float *grow = p.du + static_cast<int64_t>(tl.n) * p.du_sn + static_cast<int64_t>(i) * p.du_si;
+#pragma unroll
+                for (int sc = 0; sc < Cfg::SN; ++sc) {
+                    const int cl = co[sc];
+                    const int c = tl.c0 + cl;
+                    if (c >= p.hd) continue;
+                    float u[Cfg::VN], o[Cfg::VN];
+                    dev::Vec<Cfg::VN>::load(us + rl * Cfg::TC + cl, u);
+#pragma unroll
+                    for (int e = 0; e < Cfg::VN; ++e) o[e] = __fadd_rn(u[e], acc[sr * Cfg::VR + er][sc * Cfg::VN + e]);
+                    if (c + Cfg::VN <= p.hd) {
+                        dev::Vec<Cfg::VN>::store(grow + c, o);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < Cfg::VN; ++e)
+                            if (c + e < p.hd) grow[c + e] = o[e];
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(du_empty);
+    }
+}
+
+template <class Cfg>
+cudaError_t launch_cfg(const TmaParams &p, int grid, cudaStream_t st, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gx_tma_kernel<Cfg>, p);
+}
+
+template <class Cfg>
+ConfigInfo info_of() {
+    return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW};
+}
+
+// The tile menu: (RM, RN, WM, WN, KB, ST, MINB).
+using C0 = TCfg<8, 8, 4, 2, 32, 3, 1>;   // 128 x 128, 8 consumer warps (throughput)
+using C1 = TCfg<8, 8, 2, 2, 32, 3, 2>;   //  64 x 128, 4 warps
+using C2 = TCfg<4, 8, 2, 2, 32, 4, 2>;   //  32 x 128, 4 warps
+using C3 = TCfg<8, 8, 2, 1, 32, 4, 2>;   //  64 x  64, 2 warps
+using C4 = TCfg<4, 8, 4, 1, 32, 4, 2>;   //  64 x  64, 4 warps
+using C5 = TCfg<4, 4, 2, 2, 32, 2, 4>;   //  32 x  64, 4 warps (latency)
+using C6 = TCfg<2, 4, 2, 2, 32, 2, 4>;   //  16 x  64, 4 warps
+using C7 = TCfg<4, 4, 1, 1, 32, 2, 8>;   //  16 x  32, 1 warp
+using C8 = TCfg<2, 4, 1, 1, 32, 2, 8>;   //   8 x  32, 1 warp
+
+struct Entry {
+    ConfigInfo info;
+    const void *fn;
+    cudaError_t (*launch)(const TmaParams &, int, cudaStream_t, int);
+};
+
+#define SDMGX_ENTRY(C) Entry{info_of<C>(), reinterpret_cast<const void *>(&gx_tma_kernel<C>), &launch_cfg<C>}
+const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
+                          SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8)};
+#undef SDMGX_ENTRY
+
+}  // namespace
+
+int tma_num_configs() { return static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0])); }
+const ConfigInfo &tma_config(int k) { return kEntries[k].info; }
+const void *tma_kernel(int k) { return kEntries[k].fn; }
+cudaError_t tma_launch(int k, const TmaParams &p, int grid, cudaStream_t st, int pdl) {
+    return kEntries[k].launch(p, grid, st, pdl);
+}
+
+}  // namespace sdmgx

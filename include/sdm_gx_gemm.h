@@ -1,0 +1,199 @@
+/*
+ * sdm_gx_gemm.h -- C ABI of the GB300 (sm_103a) gx_gemm library: the deterministic FP32 per-step d_u update of a
+ * chunked backward pass.
+ *
+ * The operation (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring formula; gx_gemm_kernel's chain and
+ * epilogue): for a step ti and every chunk n = ti*P + p (0 <= p < P), row i < C and column c < hd,
+ *
+ *     acc = +0;   acc = fmaf(x[n, j, i], d_dv[n, j, c], acc)   for j = 0, 1, .., C-1   (one rounding per fma)
+ *     d_u[n, i, c] = d_u[n, i, c] + acc                                               (one more rounding)
+ *
+ * i.e. d_u(ti) += x(ti)^T d_dv(ti) with a FIXED reduction order. Every output element is produced by one GPU thread
+ * with exactly that chain on the FP32 CUDA cores (no tensor cores, no flush-to-zero), so the bits do not depend on the
+ * tiling, the launch geometry, the stream or the run, and equal a CPU evaluation of the same chain.
+ *
+ * Layout (contiguous form): x is [N, C, C] float32 with x[n, j, i] at x[(n*C + j)*C + i]; d_dv is N*C*hd float32 read
+ * as [N, C, hd] with d_dv[n, j, c] at d_dv[(n*C + j)*hd + c]; d_u is [N, C, hd] float32, updated in place. The
+ * strided entry points take element strides instead (innermost stride always 1).
+ *
+ * Ownership: the caller owns every device buffer and stream. The library never allocates or frees device memory.
+ * A plan holds raw device pointers and host memory only; it is valid while the buffers it names live.
+ *
+ * Errors: every entry point returns 0 (SDM_GX_OK) or a negative sdm_gx_status. All argument checks run before any
+ * CUDA call. An empty step (nothing to compute) returns 0 without a launch. Calls are asynchronous and
+ * stream-ordered: a kernel-side failure (a bounded device wait that gave up) is reported later by
+ * sdm_gx_device_error().
+ *
+ * Programmatic dependent launch (pdl != 0): the step kernel may start while the previous kernel on the stream is
+ * still running. Before its grid-dependency wait it reads only x and d_u(ti) (and prefetches d_dv into L2, which has
+ * no visible effect); d_dv is read, and d_u written, only after the wait. The caller vouches that the previous
+ * kernel writes neither x nor d_u(ti) (the page's step(ti, pdl=True) contract in make_step).
+ *
+ * Thread safety: entry points may be called from several host threads; per-device attributes are set once under a
+ * lock. A plan may be launched from several threads; it is not modified by launches.
+ */
+#ifndef SDM_GX_GEMM_H_
+#define SDM_GX_GEMM_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDM_GX_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define SDM_GX_API __attribute__((visibility("default")))
+#else
+#define SDM_GX_API
+#endif
+
+typedef enum sdm_gx_status {
+    SDM_GX_OK = 0,
+    SDM_GX_E_NULL = -1,          /* a required pointer argument is NULL                                          */
+    SDM_GX_E_SHAPE = -2,         /* C outside [1, 256] or hd outside [1, 2^20)                                   */
+    SDM_GX_E_RANGE = -3,         /* not 1 <= P <= N < 2^31, or not 0 <= ti < N / P (checked by division)        */
+    SDM_GX_E_ALIGN = -4,         /* an operand pointer is not 4-byte aligned                                     */
+    SDM_GX_E_OVERLAP = -5,       /* d_u overlaps x or d_dv (the in-place update needs disjoint operands)         */
+    SDM_GX_E_STRIDE = -6,        /* strides do not describe a non-overlapping [N, rows, cols] layout, or overflow */
+    SDM_GX_E_GRID = -7,          /* more than 2^31 - 1 tiles in one step                                         */
+    SDM_GX_E_SMEM = -8,          /* the kernel's shared memory exceeds the device's opt-in limit                 */
+    SDM_GX_E_DEVICE = -9,        /* an operand is not device memory of the current device                        */
+    SDM_GX_E_PLAN = -10,         /* plan pointer NULL or corrupt (bad magic / size)                              */
+    SDM_GX_E_PLAN_TI = -11,      /* ti outside [0, ti_max] of the plan                                           */
+    SDM_GX_E_PLAN_DEVICE = -12,  /* the current device is not the plan's device                                  */
+    SDM_GX_E_FLAGS = -13,        /* unknown flag bits or an invalid forced configuration                         */
+    SDM_GX_E_CUDA = -14,         /* a CUDA runtime call failed: sdm_gx_last_cuda_error() has its cudaError_t     */
+    SDM_GX_E_DEVICE_FAULT = -15, /* the device error word is set: a bounded wait inside a kernel gave up          */
+    SDM_GX_E_UNSUPPORTED = -16,  /* the current device is not compute capability 10.3 (this build is sm_103a only) */
+    SDM_GX_E_ALLOC = -17         /* host memory for a plan could not be allocated                                */
+} sdm_gx_status;
+
+/* Element strides of the three operands (innermost stride is 1 for all):
+ *   x[n, j, i]    at x    + n*x_sn  + j*x_sj  + i
+ *   d_dv[n, j, c] at d_dv + n*dv_sn + j*dv_sj + c
+ *   d_u[n, i, c]  at d_u  + n*du_sn + i*du_si + c
+ * Valid layouts: x_sj >= C, x_sn >= C*x_sj, dv_sj >= hd, dv_sn >= C*dv_sj, du_si >= hd, du_sn >= C*du_si. */
+typedef struct sdm_gx_strides {
+    int64_t x_sn, x_sj;
+    int64_t dv_sn, dv_sj;
+    int64_t du_sn, du_si;
+} sdm_gx_strides;
+
+/* Launch geometry of a plan (also what sdm_gx_gemm_geometry reports for a shape). */
+typedef struct sdm_gx_geom {
+    int32_t path;         /* 0: generic kernel (any layout), 1: TMA-fed pipelined kernel                       */
+    int32_t config;       /* index of the tile configuration within the path                                  */
+    int32_t TI;           /* rows i per tile                                                                   */
+    int32_t TC;           /* columns c per tile                                                                */
+    int32_t KB;           /* j values per shared-memory stage                                                  */
+    int32_t stages;       /* pipeline stages (TMA path) or 1                                                   */
+    int32_t threads;      /* threads per CTA                                                                   */
+    int32_t smem_bytes;   /* dynamic shared memory per CTA                                                     */
+    int64_t tiles;        /* tiles per step: P * ceil(C / TI) * ceil(hd / TC)                                   */
+    int32_t ctas;         /* CTAs launched per step (persistent: each loops over tiles)                        */
+    int32_t ctas_per_sm;  /* resident CTAs per SM at this configuration                                        */
+    int32_t sms;          /* SM count of the device                                                            */
+    int32_t one_wave;     /* 1 if every tile gets its own resident CTA (tiles <= sms * ctas_per_sm)            */
+} sdm_gx_geom;
+
+typedef struct sdm_gx_plan sdm_gx_plan;   /* opaque; host memory only */
+
+/* Flags (plan_create / step_ex). 0 selects everything automatically. */
+#define SDM_GX_FLAG_GENERIC      0x100u   /* force the generic kernel                                         */
+#define SDM_GX_FLAG_NO_PREFETCH  0x200u   /* TMA path: no L2 prefetch of d_dv before the dependency wait       */
+#define SDM_GX_FLAG_CONFIG_MASK  0x0FFu   /* (index + 1) of a forced tile configuration of the chosen path     */
+#define SDM_GX_FLAG_CTAS_SHIFT   12       /* bits 12..15: forced resident CTAs per SM (0 = automatic)          */
+#define SDM_GX_FLAG_CTAS_MASK    0xF000u
+
+/*
+ * One step ti on contiguous operands (the page's gx_gemm launcher, minus torch). d_u, x, d_dv are device pointers of
+ * the current device; the step reads x and d_dv chunks ti*P .. ti*P + P - 1 and updates the same d_u chunks.
+ * N is not known here: the caller guarantees that those chunks exist (the strided/plan entries check ti < N / P).
+ * Checks: pointers non-NULL and 4-byte aligned; 1 <= C <= 256; 1 <= hd < 2^20; P >= 1, ti >= 0 and
+ * (ti + 1) * P < 2^31; the step's d_u span does not overlap its x or d_dv span.
+ * stream: a cudaStream_t (NULL: the legacy default stream). pdl != 0: programmatic dependent launch (see above).
+ */
+SDM_GX_API int sdm_gx_gemm_step(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t P, int64_t C, int64_t hd,
+                     cudaStream_t stream, int pdl);
+
+/* One step on strided operands with the chunk count N (strides NULL: contiguous). Checks 1 <= P <= N < 2^31 and
+ * 0 <= ti < N / P, the stride rules of sdm_gx_strides, and that d_u's whole [N, C, hd] span overlaps neither x's
+ * nor d_dv's. flags: SDM_GX_FLAG_*. */
+SDM_GX_API int sdm_gx_gemm_step_ex(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t N, int64_t P, int64_t C,
+                        int64_t hd, const sdm_gx_strides *strides, cudaStream_t stream, int pdl, unsigned flags);
+
+/* The geometry a step of this shape and layout would use on the current device (no launch). */
+SDM_GX_API int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C,
+                         int64_t hd, const sdm_gx_strides *strides, unsigned flags, sdm_gx_geom *out);
+
+/*
+ * Plans (the page's gx_gemm_plan / gx_gemm_plan_launch): validate once, launch many steps with only ti changing.
+ * plan_create runs every check of sdm_gx_gemm_step_ex for ti = ti_max (which covers every ti <= ti_max), picks the
+ * kernel and tile configuration, sets the kernel attributes, and encodes the TMA descriptors of the whole tensors.
+ * *out receives a plan allocated in host memory (free it with sdm_gx_gemm_plan_destroy). The plan is bound to the
+ * current device.
+ */
+SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
+                            int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max, unsigned flags);
+
+/* Launch step ti of a plan on `stream` (pdl as above). Errors: SDM_GX_E_PLAN (NULL / corrupt plan),
+ * SDM_GX_E_PLAN_TI (ti < 0 or ti > ti_max), SDM_GX_E_PLAN_DEVICE (current device differs), SDM_GX_E_CUDA. */
+SDM_GX_API int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl);
+
+/* The multi-step driver: launch steps ti_begin, ti_begin +- 1, ... stopping before ti_end (descending when
+ * ti_begin > ti_end, e.g. (T-1, -1) for the backward's reverse loop), back to back on `stream`. With pdl != 0 every
+ * launch after the first uses programmatic dependent launch, so each step's prologue overlaps its predecessor. The
+ * first launch uses pdl as given too (its predecessor is whatever the caller enqueued before). Every ti in the range
+ * must lie in [0, ti_max]; nothing is launched otherwise. */
+SDM_GX_API int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, int64_t ti_end, cudaStream_t stream, int pdl);
+
+/* The same driver with the synthetic producer in the chain: before each step ti it launches the producer, which
+ * writes d_dv chunks of step ti from S (S has d_dv's shape and strides; see sdm_gx_producer_step). Producer and step
+ * launches alternate on `stream`; with pdl != 0 each is a programmatic dependent launch of the one before. */
+SDM_GX_API int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64_t ti_begin, int64_t ti_end,
+                                  cudaStream_t stream, int pdl);
+
+SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);
+SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
+
+/*
+ * The synthetic producer of the chained workload (not on the pages: it stands in for the kernel that writes d_dv(ti)
+ * right before each step). For chunks n = ti*P .. ti*P + P - 1: d_dv[n, j, c] = S[n, j, c] if ti is even, else
+ * -S[n, j, c] (an exact sign flip). S and d_dv are contiguous [N, C, hd] device arrays; S must not overlap d_dv.
+ * Under pdl it reads S before its dependency wait and writes d_dv after it.
+ */
+SDM_GX_API int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int64_t P, int64_t C, int64_t hd,
+                         cudaStream_t stream, int pdl);
+
+/* Registers per thread, local (spill) bytes, static shared bytes and max threads per block of a kernel:
+ * path 0 = generic (config 0..2 = 16/32/64 rows), path 1 = TMA (config index as in sdm_gx_geom). out[4]. */
+SDM_GX_API int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]);
+
+/* Number of tile configurations of a path (for sweeps and tests). */
+SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
+
+/* The device error word of the current device: nonzero bits mean a kernel gave up a bounded wait (bit 0: a consumer
+ * waited too long for staged data, bit 1: the producer waited too long for a free stage, bit 2: a drain wait gave
+ * up). Synchronizes the device. clear != 0 resets it to 0 afterwards. */
+SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
+
+/* Launches of the library's kernels since load: out[0] = step kernels, out[1] = producer kernels,
+ * out[2] = launches with programmatic dependent launch. */
+SDM_GX_API void sdm_gx_launch_counts(int64_t out[3]);
+
+/* The cudaError_t of the last SDM_GX_E_CUDA returned on this host thread (0 if none). */
+SDM_GX_API int sdm_gx_last_cuda_error(void);
+
+/* A static description of a status code. */
+SDM_GX_API const char *sdm_gx_strerror(int status);
+
+SDM_GX_API int sdm_gx_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_GX_GEMM_H_ */

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle, bit for bit (NaN as a class), on the
+seeded workloads of the gx_gemm page's step update (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring
+formula), at sizes the oracle finishes in seconds, with ragged tails, every tile configuration, misaligned and
+strided layouts, the producer chain and the programmatic-dependent-launch chain."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import DevArray, assert_bitwise
+
+pytestmark = pytest.mark.gpu
+
+gx = pytest.importorskip("fp32_gemm_gb300") if torch.cuda.is_available() else None
+
+
+def _oracle_steps(inp, P, steps, S=None):
+    du = inp["d_u"].copy()
+    dv = inp["d_dv"].copy()
+    for ti in steps:
+        if S is not None:
+            oracle.producer_step(dv, S, ti, P)
+        oracle.step(du, inp["x"], dv, ti, P)
+    return du, dv
+
+
+def _dev(inp, offset=0, row_pad=0):
+    return (DevArray(inp["d_u"], offset, row_pad), DevArray(inp["x"], offset, 0),
+            DevArray(inp["d_dv"], offset, row_pad))
+
+
+def _check_untouched(dx, dv, inp, what):
+    assert_bitwise(dx.host(), inp["x"], what + " x modified")
+    assert_bitwise(dv.host(), inp["d_dv"], what + " d_dv modified")
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    gx.device_error(clear=True)
+    yield
+    assert gx.device_error(clear=True) == 0, "a kernel gave up a bounded wait"
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+@pytest.mark.parametrize("mode", ["plan_run", "plan_step", "step", "step_ex"])
+def test_tiny_all_steps(mode, pdl):
+    w = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    du, dx, dv = _dev(inp)
+    if mode == "plan_run":
+        pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+        pl.run(pdl=pdl)
+    elif mode == "plan_step":
+        pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+        for ti in reversed(range(w.T)):
+            pl.step(ti, pdl=pdl)
+    elif mode == "step":
+        for ti in range(w.T):
+            gx.step(du.t, dx.t, dv.t, ti, w.P, pdl=pdl)
+    else:
+        for ti in range(w.T):
+            gx.step_ex(du.t, dx.t, dv.t, ti, w.P, pdl=pdl)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"tiny {mode}")
+    assert du.guards_intact() and dx.guards_intact() and dv.guards_intact()
+    _check_untouched(dx, dv, inp, "tiny")
+
+
+def _ragged_workload():
+    # C and hd not multiples of any tile; C % 4 == 0 and hd % 4 == 0 so the TMA path is eligible
+    return synth.Workload("ragged", 60, T=2, P=3, C=100, hd=76, x_scale="inv_sqrt_c")
+
+
+@pytest.mark.parametrize("config", list(range(9)))
+def test_every_tma_config_ragged(config):
+    w = _ragged_workload()
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [1, 0])
+    du, dx, dv = _dev(inp)
+    flags = gx.config_flag(config)
+    g = gx.geometry(du.t, dx.t, dv.t, w.P, flags=flags)
+    assert g["path"] == 1 and g["config"] == config
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=flags)
+    pl.run(1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"tma config {config}")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, f"tma config {config}")
+
+
+@pytest.mark.parametrize("config", [0, 1, 2])
+@pytest.mark.parametrize("shape", [(100, 76), (48, 99), (256, 3), (1, 1), (7, 130)])
+def test_every_generic_config(config, shape):
+    C, hd = shape
+    w = synth.Workload("gen", 61, T=2, P=2, C=C, hd=hd, x_scale="unit")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [0, 1])
+    du, dx, dv = _dev(inp)
+    flags = gx.FLAG_GENERIC | gx.config_flag(config)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=flags)
+    assert pl.geometry()["path"] == 0
+    pl.run(pdl=False)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"generic {config} {shape}")
+    assert du.guards_intact()
+
+
+EDGE_VARIANTS = {
+    "hd100": dict(hd=100, offset=0, row_pad=0, path=1),
+    "hd99": dict(hd=99, offset=0, row_pad=0, path=0),
+    "hd128_misaligned": dict(hd=128, offset=1, row_pad=0, path=0),
+    "hd128_ld129": dict(hd=128, offset=0, row_pad=1, path=0),
+    "hd128_ld132": dict(hd=128, offset=0, row_pad=4, path=1),
+}
+
+
+@pytest.mark.parametrize("variant", sorted(EDGE_VARIANTS))
+@pytest.mark.parametrize("vset", synth.VALUE_SETS)
+def test_edge_patterns(vset, variant):
+    v = EDGE_VARIANTS[variant]
+    w = synth.WORKLOADS["edge"]
+    inp = synth.make_inputs(w, value_set=vset, hd=v["hd"])
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    du, dx, dv = _dev(inp, offset=v["offset"], row_pad=v["row_pad"])
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    assert pl.geometry()["path"] == v["path"], pl.geometry()
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"edge {vset} {variant}")
+    assert du.guards_intact() and dx.guards_intact() and dv.guards_intact()
+    _check_untouched(dx, dv, inp, f"edge {vset} {variant}")
+    got = du.host()
+    zero = (got == 0) & ~np.isnan(got)
+    assert not np.any(np.signbit(got[zero])), "a -0 output"
+
+
+def test_producer_chain_full():
+    """T=64, P=8, C=64, hd=64; d_dv rewritten before every step by the synthetic producer; PDL chain."""
+    w = synth.WORKLOADS["producer_chain"]
+    inp = synth.make_inputs(w)
+    S = synth.make_source(w)
+    want_du, want_dv = _oracle_steps(inp, w.P, range(w.T), S=S)
+    du, dx, dv = _dev(inp)
+    Sd = torch.from_numpy(S).cuda()
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    pl.run_producer(Sd, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want_du, "producer chain d_u")
+    assert_bitwise(dv.host(), want_dv, "producer chain d_dv")
+    assert du.guards_intact() and dv.guards_intact()
+
+
+def test_pdl_chain_full():
+    """T=128, P=32, C=64, hd=128, all steps chained with PDL, reverse order."""
+    w = synth.WORKLOADS["pdl_chain"]
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    pl.run(w.T - 1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "pdl chain")
+    assert du.guards_intact()
+
+
+def test_large_two_steps():
+    """The large shape (P=256, C=128, hd=128) over two full steps, compared everywhere."""
+    w = synth.WORKLOADS["large"]
+    inp = synth.make_inputs(w, N=2 * w.P)
+    want, _ = _oracle_steps(inp, w.P, [0, 1])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "large 2 steps")
+    assert du.guards_intact()
+
+
+def test_kernel_attrs_no_spills():
+    for path in (0, 1):
+        for k in range(gx.num_configs(path)):
+            a = gx.kernel_attrs(path, k)
+            assert a["local_bytes"] == 0, (path, k, a)
+            assert a["regs"] <= 255
+
+
+def test_errors_on_device():
+    """Errors that need the device: host memory is not device memory; a plan used for a ti beyond ti_max."""
+    w = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(w)
+    du, dx, dv = _dev(inp)
+    host = torch.from_numpy(inp["d_u"].copy())
+    rc = gx.lib().sdm_gx_gemm_step(host.data_ptr(), dx.t.data_ptr(), dv.t.data_ptr(), 0, w.P, w.C, w.hd, None, 0)
+    assert gx.GxGemmError(rc, "step").name == "SDM_GX_E_DEVICE"
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, ti_max=1)
+    with pytest.raises(gx.GxGemmError) as e2:
+        pl.step(2)
+    assert e2.value.name == "SDM_GX_E_PLAN_TI"
