@@ -35,24 +35,28 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// true once the phase with the given parity has completed
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// true once the phase with the given parity has completed. A thread whose phase is not complete yet is suspended
+// (it issues nothing) until the phase completes or about hint_ns nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
-// Bounded wait: false if the phase did not complete within timeout_ns (the caller then reports and unwinds).
+// Bounded wait: false if the phase did not complete within timeout_ns (the caller then reports and unwinds). Waiting
+// threads sleep inside try_wait (suspend hint) instead of spinning, so a waiting warp leaves its issue slots to the
+// warps that compute.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    constexpr uint32_t kHintNs = 1u << 20;   // ~1 ms per suspension
+    if (mbar_try_wait(bar, parity, kHintNs)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, kHintNs)) return true;
         if (static_cast<int64_t>(global_timer_ns() - t0) > timeout_ns) return false;
     }
 }
@@ -76,6 +80,20 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t 
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- packed FP32 FMA ------------------------------------------------------------------------------------------------
+// (c0, c1) = (fma(a0, b0, c0), fma(a1, b1, c1)): one fma.rn.f32x2 instruction, each lane an IEEE fused multiply-add
+// rounded to nearest even with subnormals kept, i.e. bit for bit the same as two fmaf calls; half the issue slots.
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ---- vector shared-memory loads and global stores --------------------------------------------------------------------

@@ -39,14 +39,15 @@ struct TCfg {
     static constexpr int TC = WN * RN * LN;
     static constexpr int NCW = WM * WN;
     static constexpr int THREADS = (NCW + 1) * 32;
-    static constexpr int XS_BYTES = align_up(KB * TI * 4, 1024);
-    static constexpr int DS_BYTES = align_up(KB * TC * 4, 1024);
-    static constexpr int DU_BYTES = align_up(TI * TC * 4, 1024);
+    // every TMA destination starts on a 128-byte boundary (the dynamic shared window is aligned up to 128 bytes)
+    static constexpr int XS_BYTES = align_up(KB * TI * 4, 128);
+    static constexpr int DS_BYTES = align_up(KB * TC * 4, 128);
+    static constexpr int DU_BYTES = align_up(TI * TC * 4, 128);
     static constexpr int OFF_D = ST * XS_BYTES;
     static constexpr int OFF_U = OFF_D + ST * DS_BYTES;
     static constexpr int OFF_BAR = OFF_U + DU_BYTES;
     static constexpr int NBAR = 2 * ST + 2;
-    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8, 128) + 1024;   // + slack for 1 KB alignment
+    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8, 128) + 128;   // + slack for the 128-byte alignment
     static constexpr uint32_t STAGE_TX = static_cast<uint32_t>(KB * (TI + TC) * 4);
     static constexpr uint32_t DU_TX = static_cast<uint32_t>(TI * TC * 4);
     static constexpr int UNROLL = (RM * RN >= 64) ? 8 : ((RM * RN >= 16) ? 16 : 32);
@@ -84,10 +85,19 @@ __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const 
         for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
 #pragma unroll
         for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+        if constexpr (Cfg::RM % 2 == 0) {
+            // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
 #pragma unroll
-        for (int r = 0; r < Cfg::RM; ++r) {
+            for (int c = 0; c < Cfg::RN; ++c) {
 #pragma unroll
-            for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+                for (int r = 0; r < Cfg::RM; r += 2) dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
+            }
+        } else {
+#pragma unroll
+            for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+                for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+            }
         }
     }
 }
@@ -96,7 +106,7 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_s = dev::smem_addr(smem_raw);
-    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    const uint32_t base_s = (raw_s + 127u) & ~127u;
     unsigned char *const base_g = smem_raw + (base_s - raw_s);
     const uint32_t bar0 = base_s + Cfg::OFF_BAR;
     const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
@@ -302,6 +312,14 @@ using C5 = TCfg<4, 4, 2, 2, 32, 2, 4>;   //  32 x  64, 4 warps (latency)
 using C6 = TCfg<2, 4, 2, 2, 32, 2, 4>;   //  16 x  64, 4 warps
 using C7 = TCfg<4, 4, 1, 1, 32, 2, 8>;   //  16 x  32, 1 warp
 using C8 = TCfg<2, 4, 1, 1, 32, 2, 8>;   //   8 x  32, 1 warp
+using C9 = TCfg<4, 8, 8, 2, 32, 3, 1>;   // 128 x 128, 16 warps, 4 x 8 per thread
+using C10 = TCfg<8, 8, 4, 2, 64, 2, 1>;  // 128 x 128, 8 warps, 64 j per stage
+using C11 = TCfg<4, 8, 4, 2, 32, 3, 2>;  //  64 x 128, 8 warps, 4 x 8 per thread
+using C12 = TCfg<8, 4, 4, 4, 32, 3, 1>;  // 128 x 128, 16 warps, 8 x 4 per thread
+using C13 = TCfg<8, 8, 4, 2, 16, 3, 2>;  // 128 x 128, 8 warps, 2 CTAs per SM (<= 113 KB, <= 112 registers)
+using C14 = TCfg<8, 8, 4, 2, 16, 2, 2>;  // 128 x 128, 8 warps, 2 CTAs per SM, 2 stages
+using C15 = TCfg<8, 8, 4, 1, 32, 3, 2>;  // 128 x  64, 4 warps, 2 CTAs per SM
+using C16 = TCfg<8, 8, 2, 2, 16, 3, 3>;  //  64 x 128, 4 warps, 3 CTAs per SM
 
 struct Entry {
     ConfigInfo info;
@@ -311,7 +329,9 @@ struct Entry {
 
 #define SDMGX_ENTRY(C) Entry{info_of<C>(), reinterpret_cast<const void *>(&gx_tma_kernel<C>), &launch_cfg<C>}
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
-                          SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8)};
+                          SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
+                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13), SDMGX_ENTRY(C14),
+                          SDMGX_ENTRY(C15), SDMGX_ENTRY(C16)};
 #undef SDMGX_ENTRY
 
 }  // namespace

@@ -74,8 +74,10 @@ def _ragged_workload():
     return synth.Workload("ragged", 60, T=2, P=3, C=100, hd=76, x_scale="inv_sqrt_c")
 
 
-@pytest.mark.parametrize("config", list(range(9)))
+@pytest.mark.parametrize("config", list(range(32)))
 def test_every_tma_config_ragged(config):
+    if config >= gx.num_configs(1):
+        pytest.skip("no such configuration")
     w = _ragged_workload()
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, w.P, [1, 0])
