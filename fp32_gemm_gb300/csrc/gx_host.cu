@@ -185,32 +185,32 @@ struct Launch {
     sdm_gx_geom geom;
 };
 
-double fma_share(const ConfigInfo &ci) {
-    const int sr = std::max(1, ci.RM / 4), sn = std::max(1, ci.RN / 4);
-    return static_cast<double>(ci.RM * ci.RN) / (ci.RM * ci.RN + sr + sn);
+// The geometry rule (our re-derivation, for this kernel family, of the page's one-wave rows rule): estimate the step
+// time of every tile configuration on this device and take the fastest. A step's tiles spread over the SMs; an SM runs
+// up to `occ` CTAs at once; its FMA rate is 128 lanes x the configuration's measured efficiency x the fraction of the
+// eight-plus consumer warps it needs to reach it; each CTA also pays a per-tile cost (pipeline fill, epilogue, and the
+// j-chain's dependent-FMA latency) for every tile it runs in sequence.
+double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
+    const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+    const int64_t per_sm = (tiles + sms - 1) / sms;
+    const int64_t a = std::min<int64_t>(occ, per_sm);
+    const int64_t seq = (per_sm + a - 1) / a;
+    const double util = std::min(1.0, static_cast<double>(a * ci.consumer_warps) / 8.0);
+    const double rate = 128.0 * (ci.eff / 100.0) * util;
+    const double work = static_cast<double>(per_sm) * ci.TI * ci.TC * C;
+    return work / rate + static_cast<double>(seq) * (1500.0 + 8.0 * C);
 }
 
-// The geometry rule (our re-derivation of the page's one-wave rows rule for this kernel family): estimate the
-// step time of every tile configuration from the busiest SM's padded FMA work, the FMA share of its inner loop and
-// the number of consumer warps per SM sub-partition, plus a per-tile latency term; take the fastest.
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
     if (forced >= 0) return forced;
     double best = 1e300;
     int bk = -1;
     for (int k = 0; k < tma_num_configs(); ++k) {
         const ConfigInfo &ci = tma_config(k);
-        const int occ = d.tma_occ[k];
-        if (occ < 1) continue;
+        if (d.tma_occ[k] < 1) continue;
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
         if (tiles >= kTwo31) continue;
-        const int64_t per_sm = (tiles + d.sms - 1) / d.sms;
-        const int64_t slots = static_cast<int64_t>(d.sms) * occ;
-        const int64_t per_cta = (tiles + slots - 1) / slots;
-        const double warps = static_cast<double>(std::min<int64_t>(occ, per_sm) * ci.consumer_warps);
-        const double rate = 128.0 * fma_share(ci) * std::min(1.0, warps / 4.0);
-        const double work = static_cast<double>(per_sm) * ci.TI * ci.TC * C;
-        const double lat = static_cast<double>(per_cta) * (4.0 * C + 600.0) + 2500.0;
-        const double est = work / rate + lat;
+        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd);
         if (est < best * 0.999) {
             best = est;
             bk = k;

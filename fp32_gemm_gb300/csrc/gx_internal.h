@@ -45,6 +45,7 @@ struct GenericParams {
 
 struct ConfigInfo {
     int TI, TC, KB, stages, threads, smem, RM, RN, consumer_warps;
+    int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
 };
 
 // TMA path
