@@ -130,10 +130,11 @@ def barrier(ws):
         torch.distributed.barrier()
 
 
-def max_over_ranks(v: float, ws: int) -> float:
+def max_over_ranks(v: float, ws: int, device: str = "cuda") -> float:
+    """The maximum of a per-rank value over all ranks (the timing reduction; no data-path collective)."""
     if ws == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
@@ -213,8 +214,13 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
     gx.device_error(clear=True)
     plan = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P)
     geom = plan.geometry()
+    # the T-step chain captured once into a CUDA graph by the library (sdm_gx_gemm_plan_graph_create)
+    graph = plan.graph(0, w.T, pdl=True, S=S)
 
     def one_step():
+        graph.launch()
+
+    def one_step_direct():   # the same chain issued launch by launch by the library's C driver loop
         if S is not None:
             plan.run_producer(S, pdl=True)
         else:
@@ -235,16 +241,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
     launches = (c2["step"] - c1["step"]) + (c2["producer"] - c1["producer"])
     del c0
 
-    # producer alone (context for the producer workload): the same chain without the gemm steps is not exposed by
-    # the driver; time standalone producer launches instead
-    prod_us = None
-    if S is not None:
-        def prod_only():
-            for ti in range(w.T):
-                gx.producer_step(d["d_dv"], S, ti, w.P, pdl=True)
-        tp = time_chain(prod_only, max(1, args.steps // 2), 1, ws, stream)
-        prod_us = tp / max(1, args.steps // 2) / w.T * 1e6
-
+    t_direct = time_chain(one_step_direct, args.steps, 2, ws, stream)
     err = gx.device_error(clear=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
@@ -285,12 +282,13 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "P": w.P, "C": w.C, "hd": w.hd, "N": w.N,
-                   "step": f"{w.T} chained steps ti (PDL)" + (" with the synthetic producer" if w.producer else ""),
+                   "step": f"{w.T} chained steps ti (PDL, one CUDA graph)" + (" with the synthetic producer" if w.producer else ""),
                    "l2": f"inputs larger than L2 ({(h2d) / 1e9:.2f} GB resident)" if h2d > 129e6
                    else "inputs smaller than L2 (not flushed; latency-bound chain)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "geometry": geom},
         "us_per_step": round(per_launch_s * 1e6, 3),
+        "us_per_step_direct_launches": round(t_direct / args.steps / w.T * 1e6, 3),
         "frac_of_shape_roofline": round(roof_t / per_launch_s, 4),
         "roofline": {"bound": "alu" if F / (fp32_peak * 1e12) >= B / (hbm * 1e9) else "hbm",
                      "achieved": round(achieved_tf, 3), "peak": round(fp32_peak, 2), "unit": "TFLOP/s",
@@ -303,12 +301,10 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
                      "timing": "CUDA events over the timed region / (steps x T launches) on the launch stream"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "pinned host -> device copies, Plan.run (C ABI), d_u back to pinned host"},
+                "path": "pinned host -> device copies, the chain's graph (C ABI), d_u back to pinned host"},
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if prod_us is not None:
-        out["producer_us_per_launch"] = round(prod_us, 3)
     return out
 
 
@@ -321,6 +317,7 @@ def main():
     ap.add_argument("--workload", default="large", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=None, help="reference arm: seconds of oracle work per step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_info()
@@ -329,7 +326,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        per = max(0.5, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
+        per = args.ref_seconds if args.ref_seconds else max(0.5, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
         for _ in range(args.warmup):
             cpu_oracle_sample(w, per / 4)
         vals = [cpu_oracle_sample(w, per) for _ in range(args.steps)]

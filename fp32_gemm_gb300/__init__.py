@@ -7,7 +7,7 @@ The compute runs in the CUDA library libsdm_gx_gemm.so (C ABI: include/sdm_gx_ge
 ctypes binding. PyTorch provides device memory and streams only.
 """
 
-from ._binding import (FLAG_CONFIG_MASK, FLAG_CTAS_SHIFT, FLAG_GENERIC, FLAG_NO_PREFETCH, Geom, GxGemmError, Plan,  # noqa: F401,E501
+from ._binding import (FLAG_CONFIG_MASK, FLAG_CTAS_SHIFT, FLAG_GENERIC, FLAG_NO_PREFETCH, Geom, Graph, GxGemmError, Plan,  # noqa: F401,E501
                        Strides, abi_version, device_error, geometry, kernel_attrs, launch_counts, lib, num_configs,
                        producer_step, step, step_ex, strerror)
 from ._binding import LIB_PATH  # noqa: F401

@@ -68,6 +68,10 @@ SIGNATURES = {
     "sdm_gx_gemm_plan_run_producer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_plan_geometry": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Geom)]),
+    "sdm_gx_gemm_plan_graph_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
+    "sdm_gx_graph_launch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "sdm_gx_graph_destroy": (None, [ctypes.c_void_p]),
     "sdm_gx_gemm_plan_destroy": (None, [ctypes.c_void_p]),
     "sdm_gx_producer_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 4 +
                              [ctypes.c_void_p, ctypes.c_int]),
@@ -212,9 +216,43 @@ class Plan:
         _check(_lib.sdm_gx_gemm_plan_geometry(self._h, ctypes.byref(g)), "sdm_gx_gemm_plan_geometry")
         return g.as_dict()
 
+    def graph(self, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, S=None) -> "Graph":
+        """sdm_gx_gemm_plan_graph_create: the chain captured once into a CUDA graph (with the producer if S given)."""
+        ti_end = self.T if ti_end is None else int(ti_end)
+        if S is not None and not (S.is_cuda and S.dtype == torch.float32 and S.is_contiguous()
+                                  and S.numel() == self.N * self.C * self.hd):
+            raise ValueError("graph: S is a contiguous float32 CUDA tensor shaped like d_dv")
+        h = ctypes.c_void_p()
+        _check(_lib.sdm_gx_gemm_plan_graph_create(ctypes.byref(h), self._h, S.data_ptr() if S is not None else None,
+                                                  int(ti_begin), ti_end, int(bool(pdl))),
+               "sdm_gx_gemm_plan_graph_create")
+        return Graph(h, (self, S))
+
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:
             _lib.sdm_gx_gemm_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001
+            pass
+
+
+class Graph:
+    """An instantiated CUDA graph of a step chain (sdm_gx_graph_*). Keeps the plan and S alive."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+
+    def launch(self, stream=None) -> None:
+        _check(_lib.sdm_gx_graph_launch(self._h, _stream(stream)), "sdm_gx_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.sdm_gx_graph_destroy(self._h)
             self._h = ctypes.c_void_p()
 
     def __del__(self):

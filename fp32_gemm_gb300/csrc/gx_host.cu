@@ -33,6 +33,7 @@ constexpr int64_t kWaitTimeoutNs = 2000000000LL;   // 2 s: a healthy wait lasts 
 constexpr uint64_t kPlanMagic = 0x31504d4547584753ull;   // "SGXGEMP1"
 
 thread_local int t_last_cuda = 0;
+thread_local bool t_capturing = false;   // launches recorded into a graph are counted when the graph is launched
 std::atomic<int64_t> g_count_step{0}, g_count_producer{0}, g_count_pdl{0};
 
 int fail_cuda(cudaError_t e) {
@@ -370,8 +371,10 @@ int launch(const Launch &l, int64_t ti, cudaStream_t st, int pdl) {
         e = generic_launch(l.config, p, l.grid, st, pdl);
     }
     if (e != cudaSuccess) return fail_cuda(e);
-    g_count_step.fetch_add(1, std::memory_order_relaxed);
-    if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+    if (!t_capturing) {
+        g_count_step.fetch_add(1, std::memory_order_relaxed);
+        if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+    }
     return SDM_GX_OK;
 }
 
@@ -523,12 +526,100 @@ int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64
         cudaError_t e = producer_launch(const_cast<float *>(plan->dv), S,
                                         ti * per_step, per_step, static_cast<int>(ti & 1), stream, pdl, sms);
         if (e != cudaSuccess) return fail_cuda(e);
-        g_count_producer.fetch_add(1, std::memory_order_relaxed);
-        if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+        if (!t_capturing) {
+            g_count_producer.fetch_add(1, std::memory_order_relaxed);
+            if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+        }
         rc = launch(plan->launch, ti, stream, pdl);
         if (rc != SDM_GX_OK) return rc;
     }
     return SDM_GX_OK;
+}
+
+}  // extern "C"
+
+struct sdm_gx_graph {
+    uint64_t magic;
+    const sdm_gx_graph *self;
+    int device;
+    cudaGraphExec_t exec;
+    int64_t steps, producers, pdl_launches;   // launches one replay makes
+};
+
+namespace {
+constexpr uint64_t kGraphMagic = 0x3148504152475853ull;   // "SXGRAPH1"
+}
+
+extern "C" {
+
+int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S, int64_t ti_begin,
+                                  int64_t ti_end, int pdl) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    *out = nullptr;
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    const int64_t n = ti_begin <= ti_end ? ti_end - ti_begin : ti_begin - ti_end;
+    cudaStream_t cs = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return fail_cuda(e);
+    }
+    t_capturing = true;
+    rc = S != nullptr ? sdm_gx_gemm_plan_run_producer(plan, S, ti_begin, ti_end, cs, pdl)
+                      : sdm_gx_gemm_plan_run(plan, ti_begin, ti_end, cs, pdl);
+    t_capturing = false;
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (rc != SDM_GX_OK || e != cudaSuccess) {
+        if (g != nullptr) cudaGraphDestroy(g);
+        return rc != SDM_GX_OK ? rc : fail_cuda(e);
+    }
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail_cuda(e);
+    sdm_gx_graph *gr = static_cast<sdm_gx_graph *>(std::malloc(sizeof(sdm_gx_graph)));
+    if (gr == nullptr) {
+        cudaGraphExecDestroy(ex);
+        return SDM_GX_E_ALLOC;
+    }
+    gr->magic = kGraphMagic;
+    gr->self = gr;
+    gr->device = plan->launch.device;
+    gr->exec = ex;
+    gr->steps = n;
+    gr->producers = S != nullptr ? n : 0;
+    gr->pdl_launches = pdl ? n + gr->producers : 0;
+    *out = gr;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_graph_launch(const sdm_gx_graph *graph, cudaStream_t stream) {
+    if (graph == nullptr || graph->magic != kGraphMagic || graph->self != graph) return SDM_GX_E_PLAN;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev != graph->device) return SDM_GX_E_PLAN_DEVICE;
+    e = cudaGraphLaunch(graph->exec, stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (!t_capturing) {
+        g_count_step.fetch_add(graph->steps, std::memory_order_relaxed);
+        g_count_producer.fetch_add(graph->producers, std::memory_order_relaxed);
+        g_count_pdl.fetch_add(graph->pdl_launches, std::memory_order_relaxed);
+    }
+    return SDM_GX_OK;
+}
+
+void sdm_gx_graph_destroy(sdm_gx_graph *graph) {
+    if (graph == nullptr || graph->magic != kGraphMagic || graph->self != graph) return;
+    cudaGraphExecDestroy(graph->exec);
+    graph->magic = 0;
+    graph->self = nullptr;
+    std::free(graph);
 }
 
 int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out) {

@@ -175,9 +175,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             dev::prefetch_tensormap(&p.tm_dv);
             dev::prefetch_tensormap(&p.tm_du);
             const Tile tl = decode_tile<Cfg>(p, t);
-            dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
-            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
-            du_issued = 1;
+            // first what the first k-block needs (x now, d_dv into L2 for after the wait); the d_u box, needed only by
+            // the epilogue, goes out last so that it does not delay the first stage
             npre = nk < Cfg::ST ? nk : Cfg::ST;
             for (int s = 0; s < npre; ++s) {
                 dev::mbar_arrive_expect_tx(bar0 + 8u * s, Cfg::STAGE_TX);
@@ -186,6 +185,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             if (p.prefetch) {
                 for (int kb = 0; kb < nk; ++kb) dev::tma_prefetch_3d(&p.tm_dv, tl.c0, kb * Cfg::KB, tl.n);
             }
+            dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
+            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+            du_issued = 1;
         }
         dev::grid_dependency_wait();
         dev::launch_dependents();

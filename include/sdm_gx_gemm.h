@@ -156,6 +156,20 @@ SDM_GX_API int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, i
 SDM_GX_API int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64_t ti_begin, int64_t ti_end,
                                   cudaStream_t stream, int pdl);
 
+/*
+ * A step chain captured once into an instantiated CUDA graph (the page's per-backward plan and C++ step loop, with the
+ * host launch cost of every step paid once): the launches sdm_gx_gemm_plan_run (S == NULL) or
+ * sdm_gx_gemm_plan_run_producer (S != NULL) would issue for ti_begin .. ti_end, captured on a private stream, with
+ * programmatic-dependent-launch edges when pdl != 0. *out receives the graph (host-side handle). The graph holds the
+ * plan's pointers; it is valid while those buffers live, and on the plan's device. Creating it makes no launch.
+ */
+typedef struct sdm_gx_graph sdm_gx_graph;
+SDM_GX_API int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S,
+                                             int64_t ti_begin, int64_t ti_end, int pdl);
+/* Launch the whole captured chain on `stream` (stream-ordered, asynchronous). */
+SDM_GX_API int sdm_gx_graph_launch(const sdm_gx_graph *graph, cudaStream_t stream);
+SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
+
 SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);
 SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
 

@@ -201,3 +201,37 @@ def test_errors_on_device():
     with pytest.raises(gx.GxGemmError) as e2:
         pl.step(2)
     assert e2.value.name == "SDM_GX_E_PLAN_TI"
+
+
+def test_graph_chain_replayed_twice():
+    """The chain captured into a CUDA graph, replayed twice: every step applied twice (oracle applied twice)."""
+    w = synth.WORKLOADS["pdl_chain"]
+    inp = synth.make_inputs(w, N=8 * w.P)
+    want, _ = _oracle_steps(inp, w.P, list(range(8)) * 2)
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    g = pl.graph(7, -1, pdl=True)
+    c0 = gx.launch_counts()
+    g.launch()
+    g.launch()
+    torch.cuda.synchronize()
+    c1 = gx.launch_counts()
+    assert c1["step"] - c0["step"] == 16
+    assert_bitwise(du.host(), want, "graph chain x2")
+    assert du.guards_intact()
+    g.close()
+
+
+def test_graph_producer_chain():
+    w = synth.WORKLOADS["producer_chain"]
+    inp = synth.make_inputs(w, N=16 * w.P)
+    S = synth.make_source(w, N=16 * w.P)
+    want_du, want_dv = _oracle_steps(inp, w.P, range(16), S=S)
+    du, dx, dv = _dev(inp)
+    Sd = torch.from_numpy(S).cuda()
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    g = pl.graph(0, 16, pdl=True, S=Sd)
+    g.launch()
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want_du, "graph producer chain d_u")
+    assert_bitwise(dv.host(), want_dv, "graph producer chain d_dv")
