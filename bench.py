@@ -80,7 +80,7 @@ class ClockSampler:
         if exe is None:
             return
         self.proc = subprocess.Popen([exe, f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader",
-                                      "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                      "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
@@ -115,7 +115,7 @@ class ClockSampler:
         if not mhz:
             return None
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(mhz)}
+                "samples": len(mhz), "window": "1 s of the same chain right before the timed region, and during it"}
 
 
 def dist_info():
@@ -233,7 +233,14 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         one_step()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3 if sampler.proc is not None else 0)
+    if sampler.proc is not None:
+        # the timed region of a fast workload lasts milliseconds: keep the GPU under the same load for ~1 s while
+        # nvidia-smi samples, right before (and during) the timed region
+        time.sleep(0.2)
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            one_step()
+            torch.cuda.synchronize()
     c1 = gx.launch_counts()
     t = time_chain(one_step, args.steps, 0, ws, stream)
     c2 = gx.launch_counts()
