@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm.so")
 
 FLAG_GENERIC = 0x100
 FLAG_NO_PREFETCH = 0x200
+FLAG_TEST_STALL = 0x400
 FLAG_CONFIG_MASK = 0x0FF
 FLAG_CTAS_SHIFT = 12
 

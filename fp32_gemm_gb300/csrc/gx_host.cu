@@ -30,6 +30,7 @@ constexpr int64_t kMaxStride = int64_t(1) << 40;
 constexpr int kMaxDevices = 64;
 constexpr int kMaxConfigs = 32;
 constexpr int64_t kWaitTimeoutNs = 2000000000LL;   // 2 s: a healthy wait lasts microseconds
+constexpr int64_t kStallTestTimeoutNs = 20000000LL; // 20 ms under SDM_GX_FLAG_TEST_STALL
 constexpr uint64_t kPlanMagic = 0x31504d4547584753ull;   // "SGXGEMP1"
 
 thread_local int t_last_cuda = 0;
@@ -247,7 +248,7 @@ CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t ro
 int build_launch(float *du, const float *x, const float *dv, const Shape &sh, int64_t n_first, int64_t n_count,
                  unsigned flags, Launch *L) {
     const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
-                           SDM_GX_FLAG_CTAS_MASK;
+                           SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL;
     if (flags & ~known) return SDM_GX_E_FLAGS;
     int dev = 0;
     const DevState *dsp = nullptr;
@@ -308,8 +309,9 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         if (tiles >= kTwo31) return SDM_GX_E_GRID;
         t.ntiles = static_cast<int32_t>(tiles);
         t.prefetch = (flags & SDM_GX_FLAG_NO_PREFETCH) ? 0 : 1;
-        t.timeout_ns = kWaitTimeoutNs;
+        t.timeout_ns = (flags & SDM_GX_FLAG_TEST_STALL) ? kStallTestTimeoutNs : kWaitTimeoutNs;
         t.err = d.err;
+        t.stall_test = (flags & SDM_GX_FLAG_TEST_STALL) ? 1 : 0;
     } else {
         if (forced >= generic_num_configs()) return SDM_GX_E_FLAGS;
         const int k = choose_generic_config(d, sh.P, sh.C, sh.hd, forced);

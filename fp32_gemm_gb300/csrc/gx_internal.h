@@ -29,6 +29,7 @@ struct TmaParams {
     int32_t prefetch;       // 1: prefetch the first tile's d_dv boxes into L2 before the dependency wait
     int64_t timeout_ns;     // bound of every mbarrier wait
     uint32_t *err;          // the device error word (kErr* bits)
+    int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
 };
 
 // Parameters of the generic kernel (any strides, 4-byte alignment).

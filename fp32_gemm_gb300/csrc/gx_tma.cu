@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             npre = nk < Cfg::ST ? nk : Cfg::ST;
             for (int s = 0; s < npre; ++s) {
                 dev::mbar_arrive_expect_tx(bar0 + 8u * s, Cfg::STAGE_TX);
+                if (s == 0 && p.stall_test) continue;   // test hook: stage 0 never completes
                 dev::tma_load_3d(base_s + s * Cfg::XS_BYTES, &p.tm_x, tl.i0, s * Cfg::KB, tl.n, bar0 + 8u * s);
             }
             if (p.prefetch) {
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 const uint32_t full = bar0 + 8u * s;
                 const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
                 if (it < npre) {   // armed, x already in flight: add the d_dv box
-                    dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, kb * Cfg::KB, tl.n, full);
+                    if (!(it == 0 && p.stall_test)) dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, kb * Cfg::KB, tl.n, full);
                     continue;
                 }
                 if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 ++du_issued;
             }
         }
+        if (p.stall_test) ok = false;   // the test hook always unwinds: its consumers never took every stage
         if (!ok) {
             atomicOr(p.err, kErrProducerWait);
             // Unwind: wait for the copies this thread issued (the last use of every stage, the last d_u box), so that

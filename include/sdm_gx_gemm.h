@@ -107,6 +107,10 @@ typedef struct sdm_gx_plan sdm_gx_plan;   /* opaque; host memory only */
 #define SDM_GX_FLAG_CONFIG_MASK  0x0FFu   /* (index + 1) of a forced tile configuration of the chosen path     */
 #define SDM_GX_FLAG_CTAS_SHIFT   12       /* bits 12..15: forced resident CTAs per SM (0 = automatic)          */
 #define SDM_GX_FLAG_CTAS_MASK    0xF000u
+/* Test hook for failure detection (TMA path only): the producer arms its first stage but never issues its copies, so
+ * every wait on that stage runs out after ~20 ms instead of the normal 2 s bound. The launch then completes, leaves d_u
+ * partly unwritten, sets the device error word (read it with sdm_gx_device_error), and the context stays usable. */
+#define SDM_GX_FLAG_TEST_STALL   0x400u
 
 /*
  * One step ti on contiguous operands (the page's gx_gemm launcher, minus torch). d_u, x, d_dv are device pointers of

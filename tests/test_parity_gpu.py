@@ -235,3 +235,54 @@ def test_graph_producer_chain():
     torch.cuda.synchronize()
     assert_bitwise(du.host(), want_du, "graph producer chain d_u")
     assert_bitwise(dv.host(), want_dv, "graph producer chain d_dv")
+
+
+def test_large_full_size_bench_configuration_sampled():
+    """The large workload at full size (N = 8192, 1.6 GB), run exactly as bench.py times it (the library's CUDA graph
+    of the 32-step PDL chain); checked against the oracle on whole chunks of two steps and on 4000 random outputs."""
+    w = synth.WORKLOADS["large"]
+    inp = synth.make_inputs(w)
+    d = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
+    pl = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P)
+    assert pl.geometry() == gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P).geometry()
+    g = pl.graph(0, w.T, pdl=True)
+    g.launch()
+    torch.cuda.synchronize()
+    got = d["d_u"].cpu().numpy()
+    # whole chunks: the first chunk of step 0 and the last chunk of step T-1
+    for n in (0, w.N - 1):
+        want = inp["d_u"].copy()
+        oracle.step(want, inp["x"], inp["d_dv"], n, 1)
+        assert_bitwise(got[n], want[n], f"large chunk {n}")
+    rng = np.random.default_rng(8)
+    n = rng.integers(0, w.N, 4000)
+    i = rng.integers(0, w.C, 4000)
+    c = rng.integers(0, w.hd, 4000)
+    pts = oracle.points(inp["d_u"], inp["x"], inp["d_dv"], n, i, c)
+    assert_bitwise(got[n, i, c], pts, "large sampled outputs")
+
+
+def test_informative_cublas_cross_check():
+    """The pages' second reference: cuBLAS FP32 batched GEMM (torch.baddbmm, TF32 off) computed the same chain on the
+    configurations the page tested, but that is not a cuBLAS guarantee. Informative: report the bitwise agreement;
+    require only that both lie within the recursive-summation error bound of each other."""
+    w = synth.WORKLOADS["pdl_chain"]
+    inp = synth.make_inputs(w, N=w.P)
+    x = torch.from_numpy(inp["x"]).cuda()
+    dv = torch.from_numpy(inp["d_dv"]).cuda()
+    du = torch.from_numpy(inp["d_u"]).cuda()
+    ours = du.clone()
+    gx.Plan(ours, x, dv, w.P).step(0)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        ref = torch.baddbmm(du, x.transpose(1, 2), dv)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    torch.cuda.synchronize()
+    a, b = ours.cpu().numpy(), ref.cpu().numpy()
+    same = float(np.mean(a.view(np.uint32) == b.view(np.uint32)))
+    print(f"bitwise agreement with cuBLAS baddbmm: {same:.4f}")
+    bound = 2 * (w.C + 1) * 2.0 ** -24 * (np.abs(inp["d_u"]) + np.einsum("nji,njc->nic", np.abs(inp["x"]),
+                                                                           np.abs(inp["d_dv"])))
+    assert np.all(np.abs(a.astype(np.float64) - b) <= bound * 1.0001 + 1e-30)
