@@ -249,6 +249,12 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
     del c0
 
     t_direct = time_chain(one_step_direct, args.steps, 2, ws, stream)
+    succ_us = None
+    if args.successor and S is None:
+        succ_out = torch.empty(w.N * w.C, dtype=torch.float32, device=dev)
+        g_succ = plan.graph(0, w.T, pdl=True, succ_out=succ_out)
+        ts = time_chain(g_succ.launch, args.steps, 2, ws, stream)
+        succ_us = ts / args.steps / w.T * 1e6
     err = gx.device_error(clear=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
@@ -296,6 +302,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
                    "geometry": geom},
         "us_per_step": round(per_launch_s * 1e6, 3),
         "us_per_step_direct_launches": round(t_direct / args.steps / w.T * 1e6, 3),
+        **({"us_per_step_with_successor": round(succ_us, 3)} if succ_us is not None else {}),
         "frac_of_shape_roofline": round(roof_t / per_launch_s, 4),
         "roofline": {"bound": "alu" if F / (fp32_peak * 1e12) >= B / (hbm * 1e9) else "hbm",
                      "achieved": round(achieved_tf, 3), "peak": round(fp32_peak, 2), "unit": "TFLOP/s",
@@ -325,6 +332,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=None, help="reference arm: seconds of oracle work per step")
+    ap.add_argument("--successor", action="store_true",
+                    help="also time the chain with the synthetic successor after every step (hand-off cost)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_info()

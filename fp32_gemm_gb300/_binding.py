@@ -70,7 +70,9 @@ SIGNATURES = {
                                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_plan_geometry": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Geom)]),
     "sdm_gx_gemm_plan_graph_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_void_p,
-                                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
+                                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
+    "sdm_gx_gemm_plan_run_successor": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_graph_launch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "sdm_gx_graph_destroy": (None, [ctypes.c_void_p]),
     "sdm_gx_gemm_plan_destroy": (None, [ctypes.c_void_p]),
@@ -217,17 +219,35 @@ class Plan:
         _check(_lib.sdm_gx_gemm_plan_geometry(self._h, ctypes.byref(g)), "sdm_gx_gemm_plan_geometry")
         return g.as_dict()
 
-    def graph(self, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, S=None) -> "Graph":
-        """sdm_gx_gemm_plan_graph_create: the chain captured once into a CUDA graph (with the producer if S given)."""
+    def graph(self, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, S=None,
+              succ_out=None) -> "Graph":
+        """sdm_gx_gemm_plan_graph_create: the chain captured once into a CUDA graph (with the producer if S given, or
+        the synthetic successor if succ_out given)."""
         ti_end = self.T if ti_end is None else int(ti_end)
         if S is not None and not (S.is_cuda and S.dtype == torch.float32 and S.is_contiguous()
                                   and S.numel() == self.N * self.C * self.hd):
             raise ValueError("graph: S is a contiguous float32 CUDA tensor shaped like d_dv")
+        if succ_out is not None:
+            self._check_succ(succ_out)
         h = ctypes.c_void_p()
         _check(_lib.sdm_gx_gemm_plan_graph_create(ctypes.byref(h), self._h, S.data_ptr() if S is not None else None,
+                                                  succ_out.data_ptr() if succ_out is not None else None,
                                                   int(ti_begin), ti_end, int(bool(pdl))),
                "sdm_gx_gemm_plan_graph_create")
-        return Graph(h, (self, S))
+        return Graph(h, (self, S, succ_out))
+
+    def _check_succ(self, out) -> None:
+        if not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() == self.N * self.C):
+            raise ValueError("successor: out is a contiguous float32 CUDA tensor of N * C elements")
+
+    def run_successor(self, out, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True,
+                      stream=None) -> None:
+        """The chain with the synthetic successor (a consumer of d_u(ti): row sums into out) after every step."""
+        self._check_succ(out)
+        ti_end = self.T if ti_end is None else int(ti_end)
+        self._keep_o = out
+        _check(_lib.sdm_gx_gemm_plan_run_successor(self._h, out.data_ptr(), int(ti_begin), ti_end, _stream(stream),
+                                                   int(bool(pdl))), "sdm_gx_gemm_plan_run_successor")
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:
@@ -292,9 +312,9 @@ def device_error(clear: bool = True) -> int:
 
 
 def launch_counts() -> dict:
-    out = (ctypes.c_int64 * 3)()
+    out = (ctypes.c_int64 * 4)()
     _lib.sdm_gx_launch_counts(out)
-    return {"step": out[0], "producer": out[1], "pdl": out[2]}
+    return {"step": out[0], "producer": out[1], "pdl": out[2], "successor": out[3]}
 
 
 def strerror(status: int) -> str:

@@ -165,7 +165,49 @@ __global__ void __launch_bounds__(kProdNT) gx_producer_kernel(float *__restrict_
     }
 }
 
+// ---- synthetic successor: a consumer of d_u(ti) that runs right after the step under PDL ----------------------------
+// out[n * C + i] = d_u[n, i, 0] + d_u[n, i, 1] + ... + d_u[n, i, hd - 1] (left to right, one rounding per add) for the
+// chunks n of step ti. It triggers its dependents first (so the next step's prologue may overlap it), then waits for
+// the step that wrote d_u(ti), then reads.
+constexpr int kSuccNT = 256;
+
+__global__ void __launch_bounds__(kSuccNT) gx_successor_kernel(const float *__restrict__ du, float *__restrict__ out,
+                                                                int64_t n0, int32_t P, int32_t C, int32_t hd,
+                                                                int64_t du_sn, int64_t du_si) {
+    dev::launch_dependents();
+    dev::grid_dependency_wait();
+    const int64_t rows = static_cast<int64_t>(P) * C;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSuccNT + threadIdx.x; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * kSuccNT) {
+        const int64_t p = r / C;
+        const int64_t i = r - p * C;
+        const float *row = du + (n0 + p) * du_sn + i * du_si;
+        float s = 0.0f;
+        for (int c = 0; c < hd; ++c) s = __fadd_rn(s, row[c]);
+        out[(n0 + p) * C + i] = s;
+    }
+}
+
 }  // namespace
+
+cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int C, int hd, int64_t du_sn,
+                             int64_t du_si, cudaStream_t st, int pdl, int sms) {
+    const int64_t rows = static_cast<int64_t>(P) * C;
+    int64_t blocks = (rows + kSuccNT - 1) / kSuccNT;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kSuccNT);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gx_successor_kernel, du, out, n0, P, C, hd, du_sn, du_si);
+}
 
 int generic_num_configs() { return static_cast<int>(sizeof(kGen) / sizeof(kGen[0])); }
 const ConfigInfo &generic_config(int k) { return kGen[k].info; }

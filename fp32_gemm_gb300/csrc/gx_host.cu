@@ -35,7 +35,7 @@ constexpr uint64_t kPlanMagic = 0x31504d4547584753ull;   // "SGXGEMP1"
 
 thread_local int t_last_cuda = 0;
 thread_local bool t_capturing = false;   // launches recorded into a graph are counted when the graph is launched
-std::atomic<int64_t> g_count_step{0}, g_count_producer{0}, g_count_pdl{0};
+std::atomic<int64_t> g_count_step{0}, g_count_producer{0}, g_count_pdl{0}, g_count_succ{0};
 
 int fail_cuda(cudaError_t e) {
     t_last_cuda = static_cast<int>(e);
@@ -545,7 +545,7 @@ struct sdm_gx_graph {
     const sdm_gx_graph *self;
     int device;
     cudaGraphExec_t exec;
-    int64_t steps, producers, pdl_launches;   // launches one replay makes
+    int64_t steps, producers, successors, pdl_launches;   // launches one replay makes
 };
 
 namespace {
@@ -554,8 +554,8 @@ constexpr uint64_t kGraphMagic = 0x3148504152475853ull;   // "SXGRAPH1"
 
 extern "C" {
 
-int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S, int64_t ti_begin,
-                                  int64_t ti_end, int pdl) {
+int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S, float *succ_out,
+                                  int64_t ti_begin, int64_t ti_end, int pdl) {
     if (out == nullptr) return SDM_GX_E_NULL;
     *out = nullptr;
     int rc = plan_check(plan);
@@ -570,8 +570,15 @@ int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, c
         return fail_cuda(e);
     }
     t_capturing = true;
-    rc = S != nullptr ? sdm_gx_gemm_plan_run_producer(plan, S, ti_begin, ti_end, cs, pdl)
-                      : sdm_gx_gemm_plan_run(plan, ti_begin, ti_end, cs, pdl);
+    if (S != nullptr && succ_out != nullptr) {
+        rc = SDM_GX_E_FLAGS;   // one synthetic neighbour per chain
+    } else if (S != nullptr) {
+        rc = sdm_gx_gemm_plan_run_producer(plan, S, ti_begin, ti_end, cs, pdl);
+    } else if (succ_out != nullptr) {
+        rc = sdm_gx_gemm_plan_run_successor(plan, succ_out, ti_begin, ti_end, cs, pdl);
+    } else {
+        rc = sdm_gx_gemm_plan_run(plan, ti_begin, ti_end, cs, pdl);
+    }
     t_capturing = false;
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(cs, &g);
@@ -595,7 +602,8 @@ int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, c
     gr->exec = ex;
     gr->steps = n;
     gr->producers = S != nullptr ? n : 0;
-    gr->pdl_launches = pdl ? n + gr->producers : 0;
+    gr->successors = succ_out != nullptr ? n : 0;
+    gr->pdl_launches = pdl ? n + gr->producers + gr->successors : 0;
     *out = gr;
     return SDM_GX_OK;
 }
@@ -611,6 +619,7 @@ int sdm_gx_graph_launch(const sdm_gx_graph *graph, cudaStream_t stream) {
     if (!t_capturing) {
         g_count_step.fetch_add(graph->steps, std::memory_order_relaxed);
         g_count_producer.fetch_add(graph->producers, std::memory_order_relaxed);
+        g_count_succ.fetch_add(graph->successors, std::memory_order_relaxed);
         g_count_pdl.fetch_add(graph->pdl_launches, std::memory_order_relaxed);
     }
     return SDM_GX_OK;
@@ -622,6 +631,38 @@ void sdm_gx_graph_destroy(sdm_gx_graph *graph) {
     graph->magic = 0;
     graph->self = nullptr;
     std::free(graph);
+}
+
+int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t ti_begin, int64_t ti_end,
+                                   cudaStream_t stream, int pdl) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    if (out == nullptr) return SDM_GX_E_NULL;
+    if (reinterpret_cast<uintptr_t>(out) & 3u) return SDM_GX_E_ALIGN;
+    const Shape &sh = plan->shape;
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out);
+    const Span so{o0, o0 + static_cast<uintptr_t>(sh.N * sh.C) * 4u};
+    if (overlaps(so, span_of(plan->du, 0, sh.N, sh.s.du_sn, sh.s.du_si, sh.C, sh.hd)) ||
+        overlaps(so, span_of(plan->x, 0, sh.N, sh.s.x_sn, sh.s.x_sj, sh.C, sh.C)) ||
+        overlaps(so, span_of(plan->dv, 0, sh.N, sh.s.dv_sn, sh.s.dv_sj, sh.C, sh.hd)))
+        return SDM_GX_E_OVERLAP;
+    const int64_t step = ti_begin <= ti_end ? 1 : -1;
+    const int64_t lo = step > 0 ? ti_begin : ti_end + 1;
+    const int64_t hi = step > 0 ? ti_end - 1 : ti_begin;
+    if (ti_begin != ti_end && (lo < 0 || hi > plan->ti_max)) return SDM_GX_E_PLAN_TI;
+    const int sms = g_dev[plan->launch.device].sms;
+    for (int64_t ti = ti_begin; ti != ti_end; ti += step) {
+        rc = launch(plan->launch, ti, stream, pdl);
+        if (rc != SDM_GX_OK) return rc;
+        cudaError_t e = successor_launch(plan->du, out, ti * sh.P, static_cast<int>(sh.P), static_cast<int>(sh.C),
+                                         static_cast<int>(sh.hd), sh.s.du_sn, sh.s.du_si, stream, pdl, sms);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (!t_capturing) {
+            g_count_succ.fetch_add(1, std::memory_order_relaxed);
+            if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
+        }
+    }
+    return SDM_GX_OK;
 }
 
 int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out) {
@@ -695,11 +736,12 @@ int sdm_gx_device_error(uint32_t *word, int clear) {
     return w ? SDM_GX_E_DEVICE_FAULT : SDM_GX_OK;
 }
 
-void sdm_gx_launch_counts(int64_t out[3]) {
+void sdm_gx_launch_counts(int64_t out[4]) {
     if (out == nullptr) return;
     out[0] = g_count_step.load();
     out[1] = g_count_producer.load();
     out[2] = g_count_pdl.load();
+    out[3] = g_count_succ.load();
 }
 
 int sdm_gx_last_cuda_error(void) { return t_last_cuda; }

@@ -163,17 +163,28 @@ SDM_GX_API int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const floa
 /*
  * A step chain captured once into an instantiated CUDA graph (the page's per-backward plan and C++ step loop, with the
  * host launch cost of every step paid once): the launches sdm_gx_gemm_plan_run (S == NULL) or
- * sdm_gx_gemm_plan_run_producer (S != NULL) would issue for ti_begin .. ti_end, captured on a private stream, with
+ * sdm_gx_gemm_plan_run_producer (S != NULL) would issue for ti_begin .. ti_end, with the synthetic successor after
+ * every step when succ_out != NULL (sdm_gx_gemm_plan_run_successor), captured on a private stream, with
  * programmatic-dependent-launch edges when pdl != 0. *out receives the graph (host-side handle). The graph holds the
  * plan's pointers; it is valid while those buffers live, and on the plan's device. Creating it makes no launch.
  */
 typedef struct sdm_gx_graph sdm_gx_graph;
 SDM_GX_API int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S,
-                                             int64_t ti_begin, int64_t ti_end, int pdl);
+                                             float *succ_out, int64_t ti_begin, int64_t ti_end, int pdl);
 /* Launch the whole captured chain on `stream` (stream-ordered, asynchronous). */
 SDM_GX_API int sdm_gx_graph_launch(const sdm_gx_graph *graph, cudaStream_t stream);
 SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
 
+/*
+ * The chain with a synthetic successor after every step: step ti, then a consumer of d_u(ti) launched with programmatic
+ * dependent launch (the page's next kernel of the backward step, "Phase A", reads d_u after its own dependency wait
+ * and lets the following kernel start early; its algorithm is not built here). The successor writes
+ * out[n * C + i] = d_u[n, i, 0] + ... + d_u[n, i, hd - 1] (left to right) for the chunks of step ti; it triggers its
+ * dependents before its wait. out: device float array of N * C elements, not overlapping d_u, x or d_dv. It measures the
+ * step -> successor -> next step hand-off.
+ */
+SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t ti_begin, int64_t ti_end,
+                                              cudaStream_t stream, int pdl);
 SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);
 SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
 
@@ -199,8 +210,8 @@ SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
 SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
 
 /* Launches of the library's kernels since load: out[0] = step kernels, out[1] = producer kernels,
- * out[2] = launches with programmatic dependent launch. */
-SDM_GX_API void sdm_gx_launch_counts(int64_t out[3]);
+ * out[2] = launches with programmatic dependent launch, out[3] = successor kernels. */
+SDM_GX_API void sdm_gx_launch_counts(int64_t out[4]);
 
 /* The cudaError_t of the last SDM_GX_E_CUDA returned on this host thread (0 if none). */
 SDM_GX_API int sdm_gx_last_cuda_error(void);

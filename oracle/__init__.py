@@ -28,7 +28,8 @@ _CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-s
 _lock = threading.Lock()
 _lib = None
 
-__all__ = ["build", "lib", "fp_env_ok", "step", "run_steps", "points", "producer_step", "chunk_strides"]
+__all__ = ["build", "lib", "fp_env_ok", "step", "run_steps", "points", "producer_step", "chunk_strides",
+           "successor_rows"]
 
 
 def build(force: bool = False) -> str:
@@ -125,3 +126,14 @@ def producer_step(d_dv: np.ndarray, S: np.ndarray, ti: int, P: int) -> None:
         np.negative(S[sl], out=d_dv[sl])
     else:
         d_dv[sl] = S[sl]
+
+
+def successor_rows(d_u: np.ndarray, ti: int, P: int) -> np.ndarray:
+    """The synthetic successor (not on the pages; a stand-in for the next kernel of the backward step, which reads d_u
+    after the step): for the chunks of step ti, the row sums d_u[n, i, 0] + ... + d_u[n, i, hd-1] added left to right
+    in float32, one rounding per add. Returns float32 [P, C]."""
+    sl = d_u[ti * P:(ti + 1) * P]
+    acc = np.zeros(sl.shape[:2], np.float32)
+    for c in range(sl.shape[2]):
+        acc = acc + sl[:, :, c]          # float32 + float32: one IEEE rounding, columns in order
+    return acc

@@ -374,3 +374,20 @@ def test_golden_tiny_matches_stored_bits():
     du = inp["d_u"].copy()
     oracle.run_steps(du, inp["x"], inp["d_dv"], w.P)
     assert np.array_equal(bits(du).reshape(-1), stored)
+
+
+def test_successor_rows_pins():
+    """The synthetic successor's reference: integer rows sum exactly; a float row equals a left-to-right float32 loop
+    written independently with Python floats rounded through numpy float32 after every add."""
+    rng = np.random.default_rng(3)
+    d = rng.integers(-1000, 1000, (4, 3, 17)).astype(np.float32)
+    got = oracle.successor_rows(d, 1, 2)
+    assert np.array_equal(got.astype(np.int64), d[2:4].astype(np.int64).sum(axis=2))
+    f = rng.standard_normal((2, 2, 9)).astype(np.float32)
+    got = oracle.successor_rows(f, 0, 2)
+    for p in range(2):
+        for i in range(2):
+            s = np.float32(0.0)
+            for c in range(9):
+                s = np.float32(float(s) + float(f[p, i, c]))   # exact double sum of two floats, then one rounding
+            assert got[p, i] == s
