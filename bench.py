@@ -251,7 +251,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
     t_direct = time_chain(one_step_direct, args.steps, 2, ws, stream)
     succ_us = None
     if args.successor and S is None:
-        succ_out = torch.empty(w.N * w.C, dtype=torch.float32, device=dev)
+        succ_out = torch.empty(w.N, dtype=torch.float32, device=dev)
         g_succ = plan.graph(0, w.T, pdl=True, succ_out=succ_out)
         ts = time_chain(g_succ.launch, args.steps, 2, ws, stream)
         succ_us = ts / args.steps / w.T * 1e6

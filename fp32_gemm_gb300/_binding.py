@@ -237,12 +237,13 @@ class Plan:
         return Graph(h, (self, S, succ_out))
 
     def _check_succ(self, out) -> None:
-        if not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() == self.N * self.C):
-            raise ValueError("successor: out is a contiguous float32 CUDA tensor of N * C elements")
+        if not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous() and out.numel() == self.N):
+            raise ValueError("successor: out is a contiguous float32 CUDA tensor of N elements")
 
     def run_successor(self, out, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True,
                       stream=None) -> None:
-        """The chain with the synthetic successor (a consumer of d_u(ti): row sums into out) after every step."""
+        """The chain with the synthetic successor (a consumer of d_u(ti): each chunk's leading-row sum into out[n])
+        after every step."""
         self._check_succ(out)
         ti_end = self.T if ti_end is None else int(ti_end)
         self._keep_o = out

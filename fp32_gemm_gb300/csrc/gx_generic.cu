@@ -166,34 +166,33 @@ __global__ void __launch_bounds__(kProdNT) gx_producer_kernel(float *__restrict_
 }
 
 // ---- synthetic successor: a consumer of d_u(ti) that runs right after the step under PDL ----------------------------
-// out[n * C + i] = d_u[n, i, 0] + d_u[n, i, 1] + ... + d_u[n, i, hd - 1] (left to right, one rounding per add) for the
-// chunks n of step ti. It triggers its dependents first (so the next step's prologue may overlap it), then waits for
-// the step that wrote d_u(ti), then reads.
+// One warp per chunk n of step ti reads the chunk's leading row d_u[n, 0, :] and writes out[n] = its sum in a fixed
+// order: lane l adds d_u[n, 0, l], d_u[n, 0, l + 32], ... left to right from +0, then the 32 partial sums are combined
+// by an xor butterfly (offsets 16, 8, 4, 2, 1), one rounding per add; lane 0's value is stored. The kernel triggers
+// its dependents first (so the next step's prologue may overlap it), then waits for the step that wrote d_u(ti).
 constexpr int kSuccNT = 256;
 
 __global__ void __launch_bounds__(kSuccNT) gx_successor_kernel(const float *__restrict__ du, float *__restrict__ out,
-                                                                int64_t n0, int32_t P, int32_t C, int32_t hd,
-                                                                int64_t du_sn, int64_t du_si) {
+                                                                int64_t n0, int32_t P, int32_t hd, int64_t du_sn) {
     dev::launch_dependents();
     dev::grid_dependency_wait();
-    const int64_t rows = static_cast<int64_t>(P) * C;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kSuccNT + threadIdx.x; r < rows;
-         r += static_cast<int64_t>(gridDim.x) * kSuccNT) {
-        const int64_t p = r / C;
-        const int64_t i = r - p * C;
-        const float *row = du + (n0 + p) * du_sn + i * du_si;
-        float s = 0.0f;
-        for (int c = 0; c < hd; ++c) s = __fadd_rn(s, row[c]);
-        out[(n0 + p) * C + i] = s;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kSuccNT / 32);
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * (kSuccNT / 32) + threadIdx.x / 32; p < P; p += warps) {
+        const float *row = du + (n0 + p) * du_sn;
+        float v = 0.0f;
+        for (int c = lane; c < hd; c += 32) v = __fadd_rn(v, row[c]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if (lane == 0) out[n0 + p] = v;
     }
 }
 
 }  // namespace
 
-cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int C, int hd, int64_t du_sn,
-                             int64_t du_si, cudaStream_t st, int pdl, int sms) {
-    const int64_t rows = static_cast<int64_t>(P) * C;
-    int64_t blocks = (rows + kSuccNT - 1) / kSuccNT;
+cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int hd, int64_t du_sn, cudaStream_t st,
+                             int pdl, int sms) {
+    int64_t blocks = (static_cast<int64_t>(P) + kSuccNT / 32 - 1) / (kSuccNT / 32);
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
@@ -206,7 +205,7 @@ cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gx_successor_kernel, du, out, n0, P, C, hd, du_sn, du_si);
+    return cudaLaunchKernelEx(&cfg, gx_successor_kernel, du, out, n0, P, hd, du_sn);
 }
 
 int generic_num_configs() { return static_cast<int>(sizeof(kGen) / sizeof(kGen[0])); }

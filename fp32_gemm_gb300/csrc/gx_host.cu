@@ -641,7 +641,7 @@ int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t 
     if (reinterpret_cast<uintptr_t>(out) & 3u) return SDM_GX_E_ALIGN;
     const Shape &sh = plan->shape;
     const uintptr_t o0 = reinterpret_cast<uintptr_t>(out);
-    const Span so{o0, o0 + static_cast<uintptr_t>(sh.N * sh.C) * 4u};
+    const Span so{o0, o0 + static_cast<uintptr_t>(sh.N) * 4u};
     if (overlaps(so, span_of(plan->du, 0, sh.N, sh.s.du_sn, sh.s.du_si, sh.C, sh.hd)) ||
         overlaps(so, span_of(plan->x, 0, sh.N, sh.s.x_sn, sh.s.x_sj, sh.C, sh.C)) ||
         overlaps(so, span_of(plan->dv, 0, sh.N, sh.s.dv_sn, sh.s.dv_sj, sh.C, sh.hd)))
@@ -654,8 +654,8 @@ int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t 
     for (int64_t ti = ti_begin; ti != ti_end; ti += step) {
         rc = launch(plan->launch, ti, stream, pdl);
         if (rc != SDM_GX_OK) return rc;
-        cudaError_t e = successor_launch(plan->du, out, ti * sh.P, static_cast<int>(sh.P), static_cast<int>(sh.C),
-                                         static_cast<int>(sh.hd), sh.s.du_sn, sh.s.du_si, stream, pdl, sms);
+        cudaError_t e = successor_launch(plan->du, out, ti * sh.P, static_cast<int>(sh.P), static_cast<int>(sh.hd),
+                                         sh.s.du_sn, stream, pdl, sms);
         if (e != cudaSuccess) return fail_cuda(e);
         if (!t_capturing) {
             g_count_succ.fetch_add(1, std::memory_order_relaxed);

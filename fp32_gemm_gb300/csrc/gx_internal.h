@@ -62,8 +62,8 @@ const void *generic_kernel(int k);
 cudaError_t generic_launch(int k, const GenericParams &p, int grid, cudaStream_t st, int pdl);
 
 // synthetic successor (a consumer of d_u(ti) after the step)
-cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int C, int hd, int64_t du_sn,
-                             int64_t du_si, cudaStream_t st, int pdl, int sms);
+cudaError_t successor_launch(const float *du, float *out, int64_t n0, int P, int hd, int64_t du_sn, cudaStream_t st,
+                             int pdl, int sms);
 
 // synthetic producer
 cudaError_t producer_launch(float *dv, const float *S, int64_t base, int64_t count, int negate, cudaStream_t st,

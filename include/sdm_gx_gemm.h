@@ -177,11 +177,12 @@ SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
 
 /*
  * The chain with a synthetic successor after every step: step ti, then a consumer of d_u(ti) launched with programmatic
- * dependent launch (the page's next kernel of the backward step, "Phase A", reads d_u after its own dependency wait
- * and lets the following kernel start early; its algorithm is not built here). The successor writes
- * out[n * C + i] = d_u[n, i, 0] + ... + d_u[n, i, hd - 1] (left to right) for the chunks of step ti; it triggers its
- * dependents before its wait. out: device float array of N * C elements, not overlapping d_u, x or d_dv. It measures the
- * step -> successor -> next step hand-off.
+ * dependent launch (the page's next kernel of the backward step, "Phase A", reads token rows of d_u after its own
+ * dependency wait and lets the following kernel start early; its algorithm is not built here). For every chunk n of
+ * step ti the successor writes out[n] = the sum of the chunk's leading row d_u[n, 0, :] in a fixed order (per lane
+ * l: columns l, l + 32, ... left to right from +0; then an xor butterfly over the 32 lanes with offsets 16, 8, 4, 2, 1),
+ * and it triggers its dependents before its wait. out: device float array of N elements, not overlapping d_u, x or
+ * d_dv. It measures the step -> successor -> next step hand-off.
  */
 SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t ti_begin, int64_t ti_end,
                                               cudaStream_t stream, int pdl);

@@ -130,10 +130,16 @@ def producer_step(d_dv: np.ndarray, S: np.ndarray, ti: int, P: int) -> None:
 
 def successor_rows(d_u: np.ndarray, ti: int, P: int) -> np.ndarray:
     """The synthetic successor (not on the pages; a stand-in for the next kernel of the backward step, which reads d_u
-    after the step): for the chunks of step ti, the row sums d_u[n, i, 0] + ... + d_u[n, i, hd-1] added left to right
-    in float32, one rounding per add. Returns float32 [P, C]."""
-    sl = d_u[ti * P:(ti + 1) * P]
-    acc = np.zeros(sl.shape[:2], np.float32)
-    for c in range(sl.shape[2]):
-        acc = acc + sl[:, :, c]          # float32 + float32: one IEEE rounding, columns in order
-    return acc
+    after the step): for each chunk n of step ti, the sum of its leading row d_u[n, 0, :] in this fixed order: 32
+    partial sums, partial l = d_u[n, 0, l] + d_u[n, 0, l + 32] + ... added left to right from +0, then for offsets 16,
+    8, 4, 2, 1: partial[l] = partial[l] + partial[l ^ offset] for all l at once; the result is partial[0]. Every add
+    is one float32 rounding. Returns float32 [P]."""
+    rows = d_u[ti * P:(ti + 1) * P, 0, :]
+    hd = rows.shape[1]
+    part = np.zeros((rows.shape[0], 32), np.float32)
+    for c in range(hd):
+        part[:, c % 32] = part[:, c % 32] + rows[:, c]
+    lanes = np.arange(32)
+    for off in (16, 8, 4, 2, 1):
+        part = part + part[:, lanes ^ off]
+    return part[:, 0].copy()

@@ -377,17 +377,22 @@ def test_golden_tiny_matches_stored_bits():
 
 
 def test_successor_rows_pins():
-    """The synthetic successor's reference: integer rows sum exactly; a float row equals a left-to-right float32 loop
-    written independently with Python floats rounded through numpy float32 after every add."""
+    """The synthetic successor's reference: integer rows sum exactly; for a row of 33 floats the order is written out by
+    hand: lane 0 holds d[0] + d[32], every other lane l one value, and lane 0's butterfly result is
+    ((((p0 + p16) + (p8 + p24)) + ((p4 + p20) + (p12 + p28))) + ...) with each add rounded to float32."""
     rng = np.random.default_rng(3)
-    d = rng.integers(-1000, 1000, (4, 3, 17)).astype(np.float32)
+    d = rng.integers(-1000, 1000, (4, 3, 70)).astype(np.float32)
     got = oracle.successor_rows(d, 1, 2)
-    assert np.array_equal(got.astype(np.int64), d[2:4].astype(np.int64).sum(axis=2))
-    f = rng.standard_normal((2, 2, 9)).astype(np.float32)
-    got = oracle.successor_rows(f, 0, 2)
-    for p in range(2):
-        for i in range(2):
-            s = np.float32(0.0)
-            for c in range(9):
-                s = np.float32(float(s) + float(f[p, i, c]))   # exact double sum of two floats, then one rounding
-            assert got[p, i] == s
+    assert np.array_equal(got.astype(np.int64), d[2:4, 0].astype(np.int64).sum(axis=1))
+    f = (rng.standard_normal((1, 1, 33)) * np.exp2(rng.integers(-20, 20, (1, 1, 33)))).astype(np.float32)
+    r = f[0, 0]
+    add = lambda a, b: np.float32(float(a) + float(b))   # noqa: E731 (exact double sum of two floats, one rounding)
+    p = [add(np.float32(0.0), r[k]) for k in range(32)]
+    p[0] = add(p[0], r[32])
+
+    def level(v, off):
+        return [add(v[k], v[k ^ off]) for k in range(32)]
+    v = p
+    for off in (16, 8, 4, 2, 1):
+        v = level(v, off)
+    assert oracle.successor_rows(f, 0, 1)[0] == v[0]
