@@ -310,3 +310,58 @@ def test_successor_chain(graph):
         want_out[ti * w.P:(ti + 1) * w.P] = oracle.successor_rows(ref, ti, w.P)
     assert_bitwise(du.host(), ref, "d_u under the successor chain")
     assert_bitwise(out.cpu().numpy(), want_out, "successor row sums")
+
+
+@pytest.mark.parametrize("C,hd,P,N,path", [
+    (256, 256, 2, 4, None),      # the largest C
+    (256, 36, 1, 2, None),
+    (64, 1000, 2, 4, None),      # many column tiles
+    (12, 8, 3, 7, None),         # P does not divide N: chunk 6 is never touched
+    (96, 68, 2, 4, "generic"),
+])
+def test_corner_shapes(C, hd, P, N, path):
+    w = synth.Workload("corner", 62, T=N // P, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w, N=N)
+    T = N // P
+    want, _ = _oracle_steps(inp, P, range(T))
+    du, dx, dv = _dev(inp)
+    flags = gx.FLAG_GENERIC if path == "generic" else 0
+    pl = gx.Plan(du.t, dx.t, dv.t, P, flags=flags)
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"corner C={C} hd={hd} P={P} N={N}")
+    assert du.guards_intact()
+
+
+@pytest.mark.parametrize("x_pad,expect_path", [(4, 1), (1, 0)])
+def test_strided_x(x_pad, expect_path):
+    """x rows padded (x_sj = C + pad): a multiple-of-4 pad keeps the TMA path, an odd pad falls back to generic."""
+    w = synth.Workload("sx", 63, T=2, P=3, C=64, hd=64)
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    du = DevArray(inp["d_u"])
+    dv = DevArray(inp["d_dv"])
+    dx = DevArray(inp["x"], 0, x_pad)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    assert pl.geometry()["path"] == expect_path
+    pl.run(pdl=False)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"strided x pad {x_pad}")
+    assert dx.guards_intact()
+
+
+def test_x_and_d_dv_may_alias():
+    """x and d_dv may be the same memory (both only read); d_u may not overlap either."""
+    w = synth.Workload("alias", 64, T=2, P=2, C=32, hd=32)
+    inp = synth.make_inputs(w)
+    inp["d_dv"] = inp["x"].copy()
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    du = DevArray(inp["d_u"])
+    dx = DevArray(inp["x"])
+    pl = gx.Plan(du.t, dx.t, dx.t, w.P)
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "x aliased with d_dv")
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.Plan(dx.t, dx.t, du.t, w.P)
+    assert e.value.name == "SDM_GX_E_OVERLAP"
