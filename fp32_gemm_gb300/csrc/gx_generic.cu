@@ -116,7 +116,7 @@ cudaError_t launch_generic(const GenericParams &p, int grid, cudaStream_t st, in
 
 template <int TI>
 ConfigInfo generic_info() {
-    return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32, 40};
+    return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32, 40, 0};
 }
 
 struct GEntry {

@@ -47,6 +47,7 @@ struct DevState {
     int status = 0;
     int sms = 0, optin = 0, smem_per_sm = 0, major = 0, minor = 0;
     uint32_t *err = nullptr;
+    bool slab_ok = false;   // the driver accepts the slab kernel's 4-D x view (checked once)
     int tma_occ[kMaxConfigs] = {};
     int gen_occ[kMaxConfigs] = {};
 };
@@ -54,6 +55,19 @@ struct DevState {
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// x viewed as {32 rows, j, row block, n} (innermost first): one box of {32, KB, 4, 1} lands as four slabs of
+// [KB][32] one after the other in shared memory.
+CUresult encode_x_slabs(CUtensorMap *m, const float *base, int64_t C, int64_t chunks, int64_t sj, int64_t sn, int KB) {
+    cuuint64_t dims[4] = {32u, static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(C / 32),
+                          static_cast<cuuint64_t>(chunks)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(sj) * 4u, 128u, static_cast<cuuint64_t>(sn) * 4u};
+    cuuint32_t box[4] = {32u, static_cast<cuuint32_t>(KB), 4u, 1u};
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
 
 // Per-device setup, once (under the lock): attributes, the error word's address, every kernel's shared-memory
 // attribute and occupancy. Returns a status; *out points at the device's state.
@@ -106,6 +120,11 @@ int device_state(int *dev_out, const DevState **out) {
             if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
                 return fail_cuda(e != cudaSuccess ? e : cudaErrorNotSupported);
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        {   // encoding checks arguments only (no memory access): try the slab kernel's 4-D view on a dummy address
+            CUtensorMap probe;
+            n.slab_ok = encode_x_slabs(&probe, reinterpret_cast<const float *>(uintptr_t(1) << 20), 128, 2, 128,
+                                       128 * 128, 32) == CUDA_SUCCESS;
         }
         n.init = true;
         d = n;
@@ -194,6 +213,16 @@ struct Launch {
 // j-chain's dependent-FMA latency) for every tile it runs in sequence.
 double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
     const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+    if (ci.slab) {
+        // balanced slabs: every SM gets at most ceil(slabs / SMs), in rounds of four on 16 warps; a partial round of
+        // k slabs costs about 1 + 0.9 k slabs (measured: its fixed part does not shrink with k)
+        const int64_t per_sm = (tiles + sms - 1) / sms;
+        const int64_t full = per_sm / 4, k = per_sm % 4;
+        const double eq = 4.0 * static_cast<double>(full) + (k ? 1.0 + 0.9 * static_cast<double>(k) : 0.0);
+        const int64_t rounds = (per_sm + 3) / 4;
+        const double rate = 128.0 * (ci.eff / 100.0);
+        return eq * ci.TI * ci.TC * C / rate + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
+    }
     const int64_t per_sm = (tiles + sms - 1) / sms;
     const int64_t a = std::min<int64_t>(occ, per_sm);
     const int64_t seq = (per_sm + a - 1) / a;
@@ -203,16 +232,24 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
     return work / rate + static_cast<double>(seq) * (1500.0 + 8.0 * C);
 }
 
+// The slab kernel needs whole 32-row slabs (C % 32 == 0) and at most two (chunk, column block) per round of four
+// consecutive slabs (C / 32 >= 3).
+bool config_eligible(const ConfigInfo &ci, int64_t C) {
+    if (!ci.slab) return true;
+    return C % ci.TI == 0 && C / ci.TI >= 3;
+}
+
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
     if (forced >= 0) return forced;
     double best = 1e300;
     int bk = -1;
     for (int k = 0; k < tma_num_configs(); ++k) {
         const ConfigInfo &ci = tma_config(k);
-        if (d.tma_occ[k] < 1) continue;
+        if (d.tma_occ[k] < 1 || !config_eligible(ci, C) || (ci.slab && !d.slab_ok)) continue;
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
         if (tiles >= kTwo31) continue;
-        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd);
+        // the slab kernel must beat the best tile configuration by 5% (its model is the coarser one)
+        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd) * (ci.slab ? 1.0 / 0.95 : 1.0);
         if (est < best * 0.999) {
             best = est;
             bk = k;
@@ -285,6 +322,7 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
+        if (!config_eligible(*ci, sh.C) || (ci->slab && !d.slab_ok)) return SDM_GX_E_FLAGS;
         if (ci->smem > d.optin || d.tma_occ[k] < 1) return SDM_GX_E_SMEM;
         occ = d.tma_occ[k];
         l.path = 1;
@@ -292,10 +330,16 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         TmaParams &t = l.tma;
         std::memset(&t, 0, sizeof(t));
         CUresult r;
+        const int du_rows = ci->slab ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
         if ((r = encode_map(&t.tm_x, x0, sh.C, sh.C, n_count, s.x_sj, s.x_sn, ci->TI, ci->KB)) != CUDA_SUCCESS ||
             (r = encode_map(&t.tm_dv, dv0, sh.hd, sh.C, n_count, s.dv_sj, s.dv_sn, ci->TC, ci->KB)) !=
                 CUDA_SUCCESS ||
-            (r = encode_map(&t.tm_du, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, ci->TI)) != CUDA_SUCCESS)
+            (r = encode_map(&t.tm_du, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, du_rows)) !=
+                CUDA_SUCCESS ||
+            (ci->slab &&
+             ((r = encode_x_slabs(&t.tm_x4, x0, sh.C, n_count, s.x_sj, s.x_sn, ci->KB)) != CUDA_SUCCESS ||
+              (r = encode_map(&t.tm_du1, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, ci->TI)) !=
+                  CUDA_SUCCESS)))
             return fail_cuda(r == CUDA_ERROR_INVALID_VALUE ? cudaErrorInvalidValue : cudaErrorUnknown);
         t.du = du0;
         t.du_sn = s.du_sn;

@@ -20,6 +20,8 @@ struct TmaParams {
     CUtensorMap tm_x;
     CUtensorMap tm_dv;
     CUtensorMap tm_du;
+    CUtensorMap tm_x4;      // slab kernel: x as {32 rows, j, row block, n}, box = four 32-row slabs
+    CUtensorMap tm_du1;     // slab kernel: d_u box of one 32-row slab
     float *du;
     int64_t du_sn, du_si;
     int32_t n_base;
@@ -47,6 +49,7 @@ struct GenericParams {
 struct ConfigInfo {
     int TI, TC, KB, stages, threads, smem, RM, RN, consumer_warps;
     int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
+    int slab;   // 1: the balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3)
 };
 
 // TMA path

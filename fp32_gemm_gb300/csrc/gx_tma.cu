@@ -29,6 +29,7 @@ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 template <int RM_, int RN_, int WM_, int WN_, int KB_, int ST_, int MINB_, int EFF_>
 struct TCfg {
     static constexpr int EFF = EFF_;               // measured FMA-pipe efficiency at full occupancy, percent
+    static constexpr int SLAB = 0;
     static constexpr int RM = RM_, RN = RN_;       // per-thread tile: rows x columns
     static constexpr int WM = WM_, WN = WN_;       // consumer warps along rows / columns
     static constexpr int KB = KB_, ST = ST_;       // j rows per stage, stages
@@ -295,6 +296,277 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
 }
 
 
+
+// ---- the slab kernel: the 128 x 128 tile kernel with its work balanced over the SMs -----------------------------------
+// The step's work is cut into slabs of 32 rows x TC columns of one chunk, ordered (chunk, column block, row block), and
+// CTA b takes slabs [b S / G, (b + 1) S / G): every SM gets the same work to within one slab, so no SM idles through a
+// second round that others do not have. A CTA runs its range in rounds of four slabs; slab w of a round is computed by
+// warps 4w .. 4w + 3, one per SM sub-partition, so a partial round still loads every sub-partition evenly. When a
+// round's four slabs are consecutive row blocks of one (chunk, column block), it is staged exactly like a 128-row tile
+// (one x box of four 32-row slabs, one d_dv box, one d_u box); otherwise per slab (x, d_u) and per distinct
+// (chunk, column block) (d_dv, at most two per round: the host requires C / 32 >= 3).
+template <int KB_, int ST_, int EFF_>
+struct SCfg {
+    static constexpr int SLAB = 1;
+    static constexpr int EFF = EFF_;
+    static constexpr int RM = 8, RN = 4, KB = KB_, ST = ST_;
+    static constexpr int WS = 4, WN = 4;           // slabs per round, warps per slab
+    static constexpr int LM = 4, LN = 8;
+    static constexpr int VR = 4, SR = 2, VN = 4, SN = 1;
+    static constexpr int TI = RM * LM;             // 32 rows per slab
+    static constexpr int TC = WN * RN * LN;        // 128 columns
+    static constexpr int NCW = WS * WN;            // 16 consumer warps
+    static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int X_SLAB = KB * TI * 4;     // bytes of one slab's x rows per stage
+    static constexpr int D_BOX = KB * TC * 4;
+    static constexpr int U_SLAB = TI * TC * 4;
+    static constexpr int XS_BYTES = WS * X_SLAB;
+    static constexpr int DS_BYTES = 2 * D_BOX;     // at most two (chunk, column block) per round
+    static constexpr int OFF_D = ST * XS_BYTES;
+    static constexpr int OFF_U = OFF_D + ST * DS_BYTES;
+    static constexpr int OFF_BAR = OFF_U + WS * U_SLAB;
+    static constexpr int NBAR = 2 * ST + 2;
+    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8, 128) + 128;
+    static constexpr int UNROLL = 16;
+};
+
+struct RoundInfo {
+    int first, cnt;
+    bool full;         // four slabs, one (chunk, column block), consecutive row blocks
+    int key0, nd;      // key of the first slab; distinct keys (1 or 2)
+};
+
+__device__ __forceinline__ RoundInfo round_info(const TmaParams &p, int s_begin, int s_end, int r) {
+    RoundInfo R;
+    R.first = s_begin + 4 * r;
+    int cnt = s_end - R.first;
+    R.cnt = cnt < 0 ? 0 : (cnt > 4 ? 4 : cnt);
+    R.key0 = R.first / p.nib;
+    R.nd = R.cnt > 0 && (R.first + R.cnt - 1) / p.nib != R.key0 ? 2 : 1;
+    R.full = R.cnt == 4 && R.nd == 1;
+    return R;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void slab_coords(const TmaParams &p, int s, int32_t *n, int32_t *i0, int32_t *c0) {
+    const int key = s / p.nib;
+    const int rb = s - key * p.nib;
+    const int pp = key / p.ncb;
+    const int cb = key - pp * p.ncb;
+    *n = p.n_base + pp;
+    *i0 = rb * Cfg::TI;
+    *c0 = cb * Cfg::TC;
+}
+
+template <class Cfg>
+__device__ __forceinline__ uint32_t slab_stage_tx(const RoundInfo &R) {
+    return R.full ? static_cast<uint32_t>(Cfg::XS_BYTES + Cfg::D_BOX)
+                  : static_cast<uint32_t>(R.cnt * Cfg::X_SLAB + R.nd * Cfg::D_BOX);
+}
+
+// x (and / or) d_dv boxes of k-block kb of round R into stage buffers xs / ds, completing on `full`
+template <class Cfg>
+__device__ __forceinline__ void slab_issue(const TmaParams &p, const RoundInfo &R, int kb, uint32_t xs, uint32_t ds,
+                                           uint32_t full, bool with_x, bool with_d) {
+    int32_t n, i0, c0;
+    slab_coords<Cfg>(p, R.first, &n, &i0, &c0);
+    if (with_x) {
+        if (R.full) {
+            dev::tma_load_4d(xs, &p.tm_x4, 0, kb * Cfg::KB, i0 / Cfg::TI, n, full);
+        } else {
+            for (int w = 0; w < R.cnt; ++w) {
+                int32_t nw, iw, cw;
+                slab_coords<Cfg>(p, R.first + w, &nw, &iw, &cw);
+                dev::tma_load_3d(xs + w * Cfg::X_SLAB, &p.tm_x, iw, kb * Cfg::KB, nw, full);
+            }
+        }
+    }
+    if (with_d) {
+        dev::tma_load_3d(ds, &p.tm_dv, c0, kb * Cfg::KB, n, full);
+        if (R.nd == 2) {
+            int32_t n1, i1, c1;
+            slab_coords<Cfg>(p, R.first + R.cnt - 1, &n1, &i1, &c1);
+            dev::tma_load_3d(ds + Cfg::D_BOX, &p.tm_dv, c1, kb * Cfg::KB, n1, full);
+        }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void slab_issue_du(const TmaParams &p, const RoundInfo &R, uint32_t us, uint32_t bar) {
+    int32_t n, i0, c0;
+    slab_coords<Cfg>(p, R.first, &n, &i0, &c0);
+    if (R.full) {
+        dev::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(Cfg::WS * Cfg::U_SLAB));
+        dev::tma_load_3d(us, &p.tm_du, c0, i0, n, bar);
+    } else {
+        dev::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(R.cnt * Cfg::U_SLAB));
+        for (int w = 0; w < R.cnt; ++w) {
+            int32_t nw, iw, cw;
+            slab_coords<Cfg>(p, R.first + w, &nw, &iw, &cw);
+            dev::tma_load_3d(us + w * Cfg::U_SLAB, &p.tm_du1, cw, iw, nw, bar);
+        }
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_constant__ TmaParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_s = dev::smem_addr(smem_raw);
+    const uint32_t base_s = (raw_s + 127u) & ~127u;
+    unsigned char *const base_g = smem_raw + (base_s - raw_s);
+    const uint32_t bar0 = base_s + Cfg::OFF_BAR;
+    const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
+    const uint32_t du_empty = du_full + 8u;
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::ST; ++s) {
+            dev::mbar_init(bar0 + 8u * s, 1);
+            dev::mbar_init(bar0 + 8u * (Cfg::ST + s), Cfg::NCW);
+        }
+        dev::mbar_init(du_full, 1);
+        dev::mbar_init(du_empty, Cfg::NCW);
+        dev::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int nk = (p.C + Cfg::KB - 1) / Cfg::KB;
+    const int s_begin = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.ntiles / gridDim.x);
+    const int s_end = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.ntiles / gridDim.x);
+    const int nrounds = (s_end - s_begin + Cfg::WS - 1) / Cfg::WS;
+
+    if (warp == Cfg::NCW) {
+        // ------------------------------------------------ producer ------------------------------------------------
+        if (lane != 0) return;
+        const int total_it = nrounds * nk;
+        const int npre = total_it < Cfg::ST ? total_it : Cfg::ST;
+        int it = 0, du_issued = 0;
+        bool ok = true;
+        if (nrounds > 0) {
+            dev::prefetch_tensormap(&p.tm_x);
+            dev::prefetch_tensormap(&p.tm_x4);
+            dev::prefetch_tensormap(&p.tm_dv);
+            dev::prefetch_tensormap(&p.tm_du);
+            dev::prefetch_tensormap(&p.tm_du1);
+            for (int q = 0; q < npre; ++q) {
+                const RoundInfo Rq = round_info(p, s_begin, s_end, q / nk);
+                dev::mbar_arrive_expect_tx(bar0 + 8u * q, slab_stage_tx<Cfg>(Rq));
+                if (q == 0 && p.stall_test) continue;   // test hook: stage 0 never completes
+                slab_issue<Cfg>(p, Rq, q % nk, base_s + q * Cfg::XS_BYTES, 0u, bar0 + 8u * q, true, false);
+            }
+            const RoundInfo R0 = round_info(p, s_begin, s_end, 0);
+            if (p.prefetch) {
+                int32_t n, i0, c0;
+                slab_coords<Cfg>(p, R0.first, &n, &i0, &c0);
+                for (int kb = 0; kb < nk; ++kb) dev::tma_prefetch_3d(&p.tm_dv, c0, kb * Cfg::KB, n);
+            }
+            slab_issue_du<Cfg>(p, R0, base_s + Cfg::OFF_U, du_full);
+            du_issued = 1;
+        }
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+        for (int r = 0; r < nrounds && ok; ++r) {
+            const RoundInfo R = round_info(p, s_begin, s_end, r);
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int s = it % Cfg::ST;
+                const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+                const uint32_t full = bar0 + 8u * s;
+                const uint32_t xs = base_s + s * Cfg::XS_BYTES;
+                const uint32_t ds = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
+                if (it < npre) {
+                    if (!(it == 0 && p.stall_test)) slab_issue<Cfg>(p, R, kb, xs, ds, full, false, true);
+                    continue;
+                }
+                if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(full, slab_stage_tx<Cfg>(R));
+                slab_issue<Cfg>(p, R, kb, xs, ds, full, true, true);
+            }
+            if (ok && r > 0) {
+                if (!dev::mbar_wait(du_empty, static_cast<uint32_t>(r - 1) & 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                slab_issue_du<Cfg>(p, R, base_s + Cfg::OFF_U, du_full);
+                ++du_issued;
+            }
+        }
+        if (p.stall_test) ok = false;   // the test hook always unwinds: its consumers never took every stage
+        if (!ok) {
+            atomicOr(p.err, kErrProducerWait);
+            const int lo = it - Cfg::ST > 0 ? it - Cfg::ST : 0;
+            for (int k = lo; k < it; ++k) {
+                if (!dev::mbar_wait(bar0 + 8u * (k % Cfg::ST), static_cast<uint32_t>(k / Cfg::ST) & 1u, p.timeout_ns))
+                    atomicOr(p.err, kErrDrainWait);
+            }
+            if (du_issued > 0 && !dev::mbar_wait(du_full, static_cast<uint32_t>(du_issued - 1) & 1u, p.timeout_ns))
+                atomicOr(p.err, kErrDrainWait);
+        }
+        return;
+    }
+
+    // -------------------------------------------------- consumers --------------------------------------------------
+    const int ws = warp / Cfg::WN;   // the slab of the round this warp computes
+    const int wn = warp % Cfg::WN;   // its column group (== its sub-partition)
+    const int lm = lane / Cfg::LN;
+    const int ln = lane % Cfg::LN;
+    int ro[Cfg::SR], co[Cfg::SN];
+#pragma unroll
+    for (int s = 0; s < Cfg::SR; ++s) ro[s] = s * Cfg::VR * Cfg::LM + lm * Cfg::VR;
+    co[0] = wn * Cfg::RN * Cfg::LN + ln * Cfg::VN;
+
+    dev::grid_dependency_wait();
+    int it = 0;
+    for (int r = 0; r < nrounds; ++r) {
+        const RoundInfo R = round_info(p, s_begin, s_end, r);
+        const bool active = ws < R.cnt;
+        int32_t n, i0, c0;
+        slab_coords<Cfg>(p, active ? R.first + ws : R.first, &n, &i0, &c0);
+        const int dslot = (n - p.n_base) * p.ncb + c0 / Cfg::TC == R.key0 ? 0 : 1;
+        float acc[Cfg::RM][Cfg::RN];
+#pragma unroll
+        for (int i = 0; i < Cfg::RM; ++i) {
+#pragma unroll
+            for (int c = 0; c < Cfg::RN; ++c) acc[i][c] = 0.0f;   // +0: the chain's start value
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int s = it % Cfg::ST;
+            const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+            if (!__all_sync(0xffffffffu, dev::mbar_wait(bar0 + 8u * s, ph, p.timeout_ns))) {
+                if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+                return;
+            }
+            if (active) {
+                const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES + ws * Cfg::X_SLAB);
+                const float *ds =
+                    reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES + dslot * Cfg::D_BOX);
+                const int nj = p.C - kb * Cfg::KB;
+                if (nj >= Cfg::KB) {
+                    chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+                } else {
+                    chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+        }
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(r) & 1u, p.timeout_ns))) {
+            if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+            return;
+        }
+        if (active) {
+            const Tile tl{n, i0, c0};
+            const float *us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U + ws * Cfg::U_SLAB);
+            epilogue<Cfg>(p, tl, us, ro, co, acc);
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(du_empty);
+    }
+}
+
 template <class Cfg>
 cudaError_t launch_cfg(const TmaParams &p, int grid, cudaStream_t st, int pdl) {
     cudaLaunchConfig_t cfg = {};
@@ -307,14 +579,27 @@ cudaError_t launch_cfg(const TmaParams &p, int grid, cudaStream_t st, int pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gx_tma_kernel<Cfg>, p);
+    if constexpr (Cfg::SLAB == 1) {
+        return cudaLaunchKernelEx(&cfg, gx_slab_kernel<Cfg>, p);
+    } else {
+        return cudaLaunchKernelEx(&cfg, gx_tma_kernel<Cfg>, p);
+    }
+}
+
+template <class Cfg>
+const void *kernel_of() {
+    if constexpr (Cfg::SLAB == 1) {
+        return reinterpret_cast<const void *>(&gx_slab_kernel<Cfg>);
+    } else {
+        return reinterpret_cast<const void *>(&gx_tma_kernel<Cfg>);
+    }
 }
 
 
 template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF};
+                      Cfg::EFF, Cfg::SLAB};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
@@ -331,6 +616,7 @@ using C7 = TCfg<4, 4, 2, 2, 32, 2, 4, 60>;   //  32 x  64,  4 warps (latency-bou
 using C8 = TCfg<2, 4, 2, 2, 32, 2, 4, 28>;   //  16 x  64,  4 warps
 using C9 = TCfg<4, 4, 1, 1, 32, 2, 8, 25>;   //  16 x  32,  1 warp
 using C10 = TCfg<2, 4, 1, 1, 32, 2, 8, 20>;  //   8 x  32,  1 warp
+using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 warps (rounds of four slabs)
 
 struct Entry {
     ConfigInfo info;
@@ -338,10 +624,10 @@ struct Entry {
     cudaError_t (*launch)(const TmaParams &, int, cudaStream_t, int);
 };
 
-#define SDMGX_ENTRY(C) Entry{info_of<C>(), reinterpret_cast<const void *>(&gx_tma_kernel<C>), &launch_cfg<C>}
+#define SDMGX_ENTRY(C) Entry{info_of<C>(), kernel_of<C>(), &launch_cfg<C>}
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
-                          SDMGX_ENTRY(C10)};
+                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11)};
 #undef SDMGX_ENTRY
 
 }  // namespace

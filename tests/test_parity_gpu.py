@@ -79,6 +79,9 @@ def test_every_tma_config_ragged(config):
     if config >= gx.num_configs(1):
         pytest.skip("no such configuration")
     w = _ragged_workload()
+    if gx.kernel_attrs(1, config)["max_threads"] == 544 and config == gx.num_configs(1) - 1:
+        # the slab kernel needs whole 32-row slabs: ragged in columns and P only
+        w = synth.Workload("ragged_slab", 65, T=2, P=5, C=96, hd=76, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, w.P, [1, 0])
     du, dx, dv = _dev(inp)
@@ -365,3 +368,22 @@ def test_x_and_d_dv_may_alias():
     with pytest.raises(gx.GxGemmError) as e:
         gx.Plan(dx.t, dx.t, du.t, w.P)
     assert e.value.name == "SDM_GX_E_OVERLAP"
+
+
+@pytest.mark.parametrize("P,C,hd,T", [(256, 128, 128, 2), (37, 128, 128, 2), (7, 96, 200, 3), (160, 128, 64, 2),
+                                      (3, 128, 128, 2)])
+def test_slab_kernel_shapes(P, C, hd, T):
+    """The balanced slab kernel: full rounds (four slabs of one chunk), rounds across chunks, partial rounds, several
+    column blocks, fewer slabs than SMs."""
+    slab = gx.num_configs(1) - 1
+    w = synth.Workload("slab", 66, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, range(T))
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(slab))
+    assert pl.geometry()["config"] == slab
+    g = pl.graph(0, T, pdl=True)
+    g.launch()
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"slab P={P} C={C} hd={hd}")
+    assert du.guards_intact()
