@@ -73,6 +73,7 @@ SIGNATURES = {
                                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "sdm_gx_gemm_plan_run_successor": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_plan_run_host": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2 + [ctypes.c_void_p] * 3),
     "sdm_gx_graph_launch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "sdm_gx_graph_destroy": (None, [ctypes.c_void_p]),
     "sdm_gx_gemm_plan_destroy": (None, [ctypes.c_void_p]),
@@ -218,6 +219,25 @@ class Plan:
         g = Geom()
         _check(_lib.sdm_gx_gemm_plan_geometry(self._h, ctypes.byref(g)), "sdm_gx_gemm_plan_geometry")
         return g.as_dict()
+
+    def run_host(self, d_u_host, x_host, d_dv_host, ti_begin: int = 0, ti_end: int | None = None,
+                 compute=None, h2d=None, d2h=None) -> None:
+        """sdm_gx_gemm_plan_run_host: the chain fed from host tensors (pinned for overlap), copies overlapped with
+        compute; d_u_host is updated when `d2h` (default: the plan's own copy-out stream) has finished."""
+        for t, shape in ((x_host, (self.N, self.C, self.C)), (d_dv_host, (self.N, self.C, self.hd)),
+                         (d_u_host, (self.N, self.C, self.hd))):
+            if t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"run_host: contiguous float32 host tensors of shape {shape}")
+        if not hasattr(self, "_streams"):
+            self._streams = (torch.cuda.Stream(), torch.cuda.Stream())
+        compute = torch.cuda.current_stream() if compute is None else compute
+        h2d = self._streams[0] if h2d is None else h2d
+        d2h = self._streams[1] if d2h is None else d2h
+        ti_end = self.T if ti_end is None else int(ti_end)
+        _check(_lib.sdm_gx_gemm_plan_run_host(self._h, d_u_host.data_ptr(), x_host.data_ptr(), d_dv_host.data_ptr(),
+                                              int(ti_begin), ti_end, _stream(compute), _stream(h2d), _stream(d2h)),
+               "sdm_gx_gemm_plan_run_host")
+        return d2h
 
     def graph(self, ti_begin: int = 0, ti_end: int | None = None, pdl: bool = True, S=None,
               succ_out=None) -> "Graph":

@@ -709,6 +709,64 @@ int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t 
     return SDM_GX_OK;
 }
 
+int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const float *x_host, const float *d_dv_host,
+                              int64_t ti_begin, int64_t ti_end, cudaStream_t compute, cudaStream_t h2d,
+                              cudaStream_t d2h) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+    if (d_u_host == nullptr || x_host == nullptr || d_dv_host == nullptr) return SDM_GX_E_NULL;
+    if (compute == h2d || compute == d2h || h2d == d2h) return SDM_GX_E_FLAGS;
+    const Shape &sh = plan->shape;
+    const sdm_gx_strides c = contiguous(sh.C, sh.hd);
+    if (std::memcmp(&c, &sh.s, sizeof(c)) != 0) return SDM_GX_E_STRIDE;
+    const int64_t step = ti_begin <= ti_end ? 1 : -1;
+    const int64_t lo = step > 0 ? ti_begin : ti_end + 1;
+    const int64_t hi = step > 0 ? ti_end - 1 : ti_begin;
+    if (ti_begin != ti_end && (lo < 0 || hi > plan->ti_max)) return SDM_GX_E_PLAN_TI;
+    const size_t xs = static_cast<size_t>(sh.P * sh.C * sh.C) * 4u;    // bytes of one step's x chunks
+    const size_t vs = static_cast<size_t>(sh.P * sh.C * sh.hd) * 4u;   // bytes of one step's d_dv / d_u chunks
+    cudaError_t e = cudaSuccess;
+    {   // this call's copies in start after the work already on `compute` and `d2h` (an earlier call's last steps and
+        // copies out still use the device tensors)
+        cudaEvent_t prev_c = nullptr, prev_o = nullptr;
+        if ((e = cudaEventCreateWithFlags(&prev_c, cudaEventDisableTiming)) != cudaSuccess) return fail_cuda(e);
+        if ((e = cudaEventCreateWithFlags(&prev_o, cudaEventDisableTiming)) != cudaSuccess) {
+            cudaEventDestroy(prev_c);
+            return fail_cuda(e);
+        }
+        if ((e = cudaEventRecord(prev_c, compute)) == cudaSuccess && (e = cudaEventRecord(prev_o, d2h)) == cudaSuccess &&
+            (e = cudaStreamWaitEvent(h2d, prev_c, 0)) == cudaSuccess)
+            e = cudaStreamWaitEvent(h2d, prev_o, 0);
+        cudaEventDestroy(prev_c);
+        cudaEventDestroy(prev_o);
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    for (int64_t ti = ti_begin; ti != ti_end && e == cudaSuccess; ti += step) {
+        const size_t ox = static_cast<size_t>(ti) * xs / 4u, ov = static_cast<size_t>(ti) * vs / 4u;
+        cudaEvent_t in = nullptr, done = nullptr;
+        if ((e = cudaEventCreateWithFlags(&in, cudaEventDisableTiming)) != cudaSuccess) break;
+        if ((e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming)) != cudaSuccess) {
+            cudaEventDestroy(in);
+            break;
+        }
+        if ((e = cudaMemcpyAsync(const_cast<float *>(plan->x) + ox, x_host + ox, xs, cudaMemcpyHostToDevice, h2d)) ==
+                cudaSuccess &&
+            (e = cudaMemcpyAsync(const_cast<float *>(plan->dv) + ov, d_dv_host + ov, vs, cudaMemcpyHostToDevice,
+                                 h2d)) == cudaSuccess &&
+            (e = cudaMemcpyAsync(plan->du + ov, d_u_host + ov, vs, cudaMemcpyHostToDevice, h2d)) == cudaSuccess &&
+            (e = cudaEventRecord(in, h2d)) == cudaSuccess && (e = cudaStreamWaitEvent(compute, in, 0)) == cudaSuccess) {
+            rc = launch(plan->launch, ti, compute, 0);
+            if (rc == SDM_GX_OK && (e = cudaEventRecord(done, compute)) == cudaSuccess &&
+                (e = cudaStreamWaitEvent(d2h, done, 0)) == cudaSuccess)
+                e = cudaMemcpyAsync(d_u_host + ov, plan->du + ov, vs, cudaMemcpyDeviceToHost, d2h);
+        }
+        cudaEventDestroy(in);     // released once the pending work that uses it has completed
+        cudaEventDestroy(done);
+        if (rc != SDM_GX_OK) return rc;
+    }
+    return e == cudaSuccess ? SDM_GX_OK : fail_cuda(e);
+}
+
 int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out) {
     if (out == nullptr) return SDM_GX_E_NULL;
     if (plan == nullptr || plan->magic != kPlanMagic || plan->self != plan) return SDM_GX_E_PLAN;

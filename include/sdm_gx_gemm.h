@@ -186,6 +186,19 @@ SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
  */
 SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t ti_begin, int64_t ti_end,
                                               cudaStream_t stream, int pdl);
+/*
+ * The chain fed from host memory, with copies and compute overlapped: for every step ti (in the order ti_begin,
+ * ti_begin +- 1, .. as sdm_gx_gemm_plan_run) the step's slices of x, d_dv and d_u are copied from the host arrays into
+ * the plan's device tensors on stream `h2d`, the step runs on `compute` once they have arrived, and the step's d_u
+ * slice is copied back to d_u_host on stream `d2h` once the step is done. While step ti computes, the copies of step
+ * ti + 1 in and of step ti - 1 out proceed. The host arrays have the plan's logical shapes, contiguous
+ * (x_host [N][C][C], d_dv_host and d_u_host [N][C][hd]); the plan's device tensors must be contiguous too. Use pinned
+ * host memory for the copies to run asynchronously. Returns once everything is enqueued; the caller synchronises on
+ * `d2h` (which ends with the last copy back). The three streams must be distinct.
+ */
+SDM_GX_API int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const float *x_host,
+                                         const float *d_dv_host, int64_t ti_begin, int64_t ti_end,
+                                         cudaStream_t compute, cudaStream_t h2d, cudaStream_t d2h);
 SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);
 SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
 

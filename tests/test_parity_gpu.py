@@ -387,3 +387,21 @@ def test_slab_kernel_shapes(P, C, hd, T):
     torch.cuda.synchronize()
     assert_bitwise(du.host(), want, f"slab P={P} C={C} hd={hd}")
     assert du.guards_intact()
+
+
+def test_run_host_overlapped_copies():
+    """sdm_gx_gemm_plan_run_host: the chain fed from pinned host memory with copies overlapped; d_u comes back to the
+    host array. Two calls in a row (the second starts from the first's result) match the oracle applied twice."""
+    w = synth.WORKLOADS["pdl_chain"]
+    T = 6
+    inp = synth.make_inputs(w, N=T * w.P)
+    want, _ = _oracle_steps(inp, w.P, list(range(T)) * 2)
+    host = {k: torch.from_numpy(v.copy()).pin_memory() for k, v in inp.items()}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    pl = gx.Plan(dev["d_u"], dev["x"], dev["d_dv"], w.P)
+    d2h = pl.run_host(host["d_u"], host["x"], host["d_dv"])
+    d2h = pl.run_host(host["d_u"], host["x"], host["d_dv"])
+    d2h.synchronize()
+    torch.cuda.synchronize()
+    assert_bitwise(host["d_u"].numpy(), want, "run_host x2")
+    assert_bitwise(host["x"].numpy(), inp["x"], "x host unchanged")
