@@ -741,29 +741,37 @@ int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const fl
         cudaEventDestroy(prev_o);
         if (e != cudaSuccess) return fail_cuda(e);
     }
-    for (int64_t ti = ti_begin; ti != ti_end && e == cudaSuccess; ti += step) {
-        const size_t ox = static_cast<size_t>(ti) * xs / 4u, ov = static_cast<size_t>(ti) * vs / 4u;
+    // consecutive steps are contiguous in memory: copy them in groups of about 16 MB, so that small steps do not
+    // pay a copy's fixed cost each
+    const int64_t per_step = static_cast<int64_t>(xs + 2 * vs);
+    const int64_t group = std::max<int64_t>(1, (int64_t(16) << 20) / per_step);
+    int64_t ti = ti_begin;
+    while (ti != ti_end && e == cudaSuccess && rc == SDM_GX_OK) {
+        int64_t cnt = step > 0 ? std::min(group, ti_end - ti) : std::min(group, ti - ti_end);
+        const int64_t first = step > 0 ? ti : ti - cnt + 1;   // lowest step of the group (its memory starts there)
+        const size_t ox = static_cast<size_t>(first) * xs / 4u, ov = static_cast<size_t>(first) * vs / 4u;
+        const size_t nx = static_cast<size_t>(cnt) * xs, nv = static_cast<size_t>(cnt) * vs;
         cudaEvent_t in = nullptr, done = nullptr;
         if ((e = cudaEventCreateWithFlags(&in, cudaEventDisableTiming)) != cudaSuccess) break;
         if ((e = cudaEventCreateWithFlags(&done, cudaEventDisableTiming)) != cudaSuccess) {
             cudaEventDestroy(in);
             break;
         }
-        if ((e = cudaMemcpyAsync(const_cast<float *>(plan->x) + ox, x_host + ox, xs, cudaMemcpyHostToDevice, h2d)) ==
+        if ((e = cudaMemcpyAsync(const_cast<float *>(plan->x) + ox, x_host + ox, nx, cudaMemcpyHostToDevice, h2d)) ==
                 cudaSuccess &&
-            (e = cudaMemcpyAsync(const_cast<float *>(plan->dv) + ov, d_dv_host + ov, vs, cudaMemcpyHostToDevice,
+            (e = cudaMemcpyAsync(const_cast<float *>(plan->dv) + ov, d_dv_host + ov, nv, cudaMemcpyHostToDevice,
                                  h2d)) == cudaSuccess &&
-            (e = cudaMemcpyAsync(plan->du + ov, d_u_host + ov, vs, cudaMemcpyHostToDevice, h2d)) == cudaSuccess &&
+            (e = cudaMemcpyAsync(plan->du + ov, d_u_host + ov, nv, cudaMemcpyHostToDevice, h2d)) == cudaSuccess &&
             (e = cudaEventRecord(in, h2d)) == cudaSuccess && (e = cudaStreamWaitEvent(compute, in, 0)) == cudaSuccess) {
-            rc = launch(plan->launch, ti, compute, 0);
+            for (int64_t k = 0; k < cnt && rc == SDM_GX_OK; ++k, ti += step) rc = launch(plan->launch, ti, compute, 0);
             if (rc == SDM_GX_OK && (e = cudaEventRecord(done, compute)) == cudaSuccess &&
                 (e = cudaStreamWaitEvent(d2h, done, 0)) == cudaSuccess)
-                e = cudaMemcpyAsync(d_u_host + ov, plan->du + ov, vs, cudaMemcpyDeviceToHost, d2h);
+                e = cudaMemcpyAsync(d_u_host + ov, plan->du + ov, nv, cudaMemcpyDeviceToHost, d2h);
         }
         cudaEventDestroy(in);     // released once the pending work that uses it has completed
         cudaEventDestroy(done);
-        if (rc != SDM_GX_OK) return rc;
     }
+    if (rc != SDM_GX_OK) return rc;
     return e == cudaSuccess ? SDM_GX_OK : fail_cuda(e);
 }
 

@@ -190,8 +190,9 @@ SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *ou
  * The chain fed from host memory, with copies and compute overlapped: for every step ti (in the order ti_begin,
  * ti_begin +- 1, .. as sdm_gx_gemm_plan_run) the step's slices of x, d_dv and d_u are copied from the host arrays into
  * the plan's device tensors on stream `h2d`, the step runs on `compute` once they have arrived, and the step's d_u
- * slice is copied back to d_u_host on stream `d2h` once the step is done. While step ti computes, the copies of step
- * ti + 1 in and of step ti - 1 out proceed. The host arrays have the plan's logical shapes, contiguous
+ * slice is copied back to d_u_host on stream `d2h` once the step is done (consecutive steps are copied together in
+ * groups of about 16 MB). While a group computes, the next group's copies in and the previous group's copies out
+ * proceed. A call's copies in start after the work already enqueued on `compute` and `d2h`. The host arrays have the plan's logical shapes, contiguous
  * (x_host [N][C][C], d_dv_host and d_u_host [N][C][hd]); the plan's device tensors must be contiguous too. Use pinned
  * host memory for the copies to run asynchronously. Returns once everything is enqueued; the caller synchronises on
  * `d2h` (which ends with the last copy back). The three streams must be distinct.
