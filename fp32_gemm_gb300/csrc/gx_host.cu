@@ -241,14 +241,43 @@ bool config_eligible(const ConfigInfo &ci, int64_t C) {
 
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
     if (forced >= 0) return forced;
+    auto tiles_of = [&](const ConfigInfo &ci) {
+        return P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+    };
+    auto usable = [&](int k) {
+        const ConfigInfo &ci = tma_config(k);
+        return d.tma_occ[k] >= 1 && config_eligible(ci, C) && !(ci.slab && !d.slab_ok) && tiles_of(ci) < kTwo31;
+    };
+    // Small steps (no tile of 32+ outputs per thread fills the SMs): the step is bound by latency, and the measured
+    // best is the configuration with the most tiles that still fit one wave (one tile per SM), i.e. the most
+    // parallel chains of the least work each; ties go to the more efficient configuration.
+    bool throughput = false;
+    for (int k = 0; k < tma_num_configs(); ++k) {
+        const ConfigInfo &ci = tma_config(k);
+        if (usable(k) && ci.RM * ci.RN >= 32 && tiles_of(ci) >= d.sms) throughput = true;
+    }
+    if (!throughput) {
+        int bk = -1;
+        int64_t bt = 0;
+        for (int k = 0; k < tma_num_configs(); ++k) {
+            if (!usable(k)) continue;
+            const ConfigInfo &ci = tma_config(k);
+            const int64_t t = tiles_of(ci);
+            if (t > d.sms) continue;
+            if (bk < 0 || t > bt || (t == bt && ci.eff > tma_config(bk).eff)) {
+                bk = k;
+                bt = t;
+            }
+        }
+        if (bk >= 0) return bk;
+    }
+    // Otherwise the throughput estimate of every configuration; the slab kernel must beat the best tile
+    // configuration by 5% (its model is the coarser one).
     double best = 1e300;
     int bk = -1;
     for (int k = 0; k < tma_num_configs(); ++k) {
+        if (!usable(k)) continue;
         const ConfigInfo &ci = tma_config(k);
-        if (d.tma_occ[k] < 1 || !config_eligible(ci, C) || (ci.slab && !d.slab_ok)) continue;
-        const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
-        if (tiles >= kTwo31) continue;
-        // the slab kernel must beat the best tile configuration by 5% (its model is the coarser one)
         const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd) * (ci.slab ? 1.0 / 0.95 : 1.0);
         if (est < best * 0.999) {
             best = est;

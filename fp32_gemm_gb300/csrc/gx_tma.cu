@@ -605,7 +605,7 @@ ConfigInfo info_of() {
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
 // host's geometry rule: for the larger tiles it is what the configuration reached on a GB300 with every SM busy; for
 // the small latency-oriented tiles it was fitted so that the rule reproduces the measured ordering of small steps.
-using C0 = TCfg<8, 4, 4, 4, 32, 3, 1, 75>;   // 128 x 128, 16 consumer warps, 8 x 4 per thread
+using C0 = TCfg<8, 4, 4, 4, 16, 4, 1, 75>;   // 128 x 128, 16 consumer warps, 8 x 4 per thread
 using C1 = TCfg<8, 8, 4, 2, 32, 3, 1, 73>;   // 128 x 128,  8 warps, 8 x 8 per thread
 using C2 = TCfg<8, 8, 4, 1, 32, 3, 2, 70>;   // 128 x  64,  4 warps
 using C3 = TCfg<8, 8, 2, 2, 32, 3, 2, 70>;   //  64 x 128,  4 warps
