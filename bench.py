@@ -208,6 +208,14 @@ def cpu_oracle_sample(w: synth.Workload, budget_s: float) -> dict:
             "seconds": el, "us_per_step_equiv": (w.flops_per_step() / (gflops * 1e9)) * 1e6}
 
 
+def kernel_name(gx, geom: dict) -> str:
+    """The CUDA kernel a plan of this geometry launches per step."""
+    if geom["path"] != 1:
+        return "gx_generic_kernel"
+    return {"tile": "gx_tma_kernel", "slab": "gx_slab_kernel", "stream": "gx_stream_kernel"}[
+        gx.config_info(1, geom["config"])["kind"]]
+
+
 def traffic_record():
     try:
         with open(TRAFFIC_FILE) as f:
@@ -344,7 +352,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         roof_main, roof_other = {"bound": "hbm", **mem}, {"bound": "alu", **alu}
     rec = traffic_record()
     traffic = None
-    if rec is not None and rec.get("workload") == w.name:
+    if rec is not None and rec.get("workload") == w.name and rec.get("kernel", "").startswith(kernel_name(gx, geom)):
         traffic = rec.get("bytes_per_launch")
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -361,7 +369,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         **({"us_per_step_with_successor": round(succ_us, 3)} if succ_us is not None else {}),
         "frac_of_shape_roofline": round(roof_t / per_launch_s, 4),
         "roofline": {**roof_main, "traffic": traffic, "other": roof_other,
-                     "kernel": "gx_tma_kernel" if geom["path"] == 1 else "gx_generic_kernel",
+                     "kernel": kernel_name(gx, geom),
                      "timing": "CUDA events over the timed region / (steps x T launches) on the launch stream"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,

@@ -63,6 +63,11 @@ SIGNATURES = {
                              [ctypes.POINTER(Strides), ctypes.c_uint, ctypes.POINTER(Geom)]),
     "sdm_gx_gemm_plan_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p)] + [ctypes.c_void_p] * 3 +
                                 [ctypes.c_int64] * 4 + [ctypes.POINTER(Strides), ctypes.c_int64, ctypes.c_uint]),
+    "sdm_gx_gemm_plan_create_ws": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p)] + [ctypes.c_void_p] * 3 +
+                                   [ctypes.c_int64] * 4 + [ctypes.POINTER(Strides), ctypes.c_int64, ctypes.c_uint,
+                                                           ctypes.c_void_p, ctypes.c_size_t]),
+    "sdm_gx_gemm_plan_workspace_size": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
+                                        [ctypes.POINTER(Strides), ctypes.c_uint, ctypes.POINTER(ctypes.c_size_t)]),
     "sdm_gx_gemm_plan_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_plan_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_int]),
@@ -81,6 +86,9 @@ SIGNATURES = {
                              [ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_kernel_attrs": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]),
     "sdm_gx_gemm_num_configs": (ctypes.c_int, [ctypes.c_int32]),
+    "sdm_gx_gemm_config_info": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "sdm_gx_gemm_stream_piece": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "sdm_gx_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "sdm_gx_launch_counts": (None, [ctypes.POINTER(ctypes.c_int64)]),
     "sdm_gx_last_cuda_error": (ctypes.c_int, []),
@@ -176,21 +184,45 @@ def geometry(d_u, x, d_dv, P: int, flags: int = 0) -> dict:
     return g.as_dict()
 
 
+def workspace_size(d_u, x, d_dv, P: int, flags: int = 0) -> int:
+    """sdm_gx_gemm_plan_workspace_size: bytes of plan workspace that let this shape use the stream kernel (0: none)."""
+    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    n = ctypes.c_size_t(0)
+    _check(_lib.sdm_gx_gemm_plan_workspace_size(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd,
+                                                ctypes.byref(s), int(flags), ctypes.byref(n)),
+           "sdm_gx_gemm_plan_workspace_size")
+    return int(n.value)
+
+
 class Plan:
     """sdm_gx_gemm_plan_*: validated once, launched per step with only ti changing. Keeps references to the tensors
-    so that their memory outlives the plan."""
+    so that their memory outlives the plan. workspace=True (default) gives the plan the device workspace
+    sdm_gx_gemm_plan_workspace_size asks for (a torch allocation held by the plan), so it may use the stream kernel;
+    workspace=False creates it without one (sdm_gx_gemm_plan_create)."""
 
-    def __init__(self, d_u, x, d_dv, P: int, ti_max: int | None = None, flags: int = 0):
+    def __init__(self, d_u, x, d_dv, P: int, ti_max: int | None = None, flags: int = 0, workspace: bool = True):
         uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
         self._keep = (d_u, x, d_dv)
         self.N, self.P, self.C, self.hd = N, int(P), C, hd
         self.T = N // int(P) if P >= 1 else 0
         self.ti_max = self.T - 1 if ti_max is None else int(ti_max)
         h = ctypes.c_void_p()
-        _check(_lib.sdm_gx_gemm_plan_create(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
-                                            int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags)),
-               "sdm_gx_gemm_plan_create")
+        nws = workspace_size(d_u, x, d_dv, P, flags) if workspace else 0
+        if nws > 0:
+            self._ws = torch.empty(nws, dtype=torch.uint8, device=uv.device)
+            _check(_lib.sdm_gx_gemm_plan_create_ws(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
+                                                   int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags),
+                                                   self._ws.data_ptr(), nws), "sdm_gx_gemm_plan_create_ws")
+        else:
+            self._ws = None
+            _check(_lib.sdm_gx_gemm_plan_create(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
+                                                int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags)),
+                   "sdm_gx_gemm_plan_create")
         self._h = h
+
+    @property
+    def workspace_bytes(self) -> int:
+        return 0 if self._ws is None else int(self._ws.numel())
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -317,6 +349,31 @@ def kernel_attrs(path: int, config: int) -> dict:
     out = (ctypes.c_int64 * 4)()
     _check(_lib.sdm_gx_gemm_kernel_attrs(int(path), int(config), out), "sdm_gx_gemm_kernel_attrs")
     return {"regs": out[0], "local_bytes": out[1], "static_smem": out[2], "max_threads": out[3]}
+
+
+CONFIG_KINDS = {0: "tile", 1: "slab", 2: "stream"}
+
+
+def config_info(path: int, config: int) -> dict:
+    """sdm_gx_gemm_config_info: the static description of a configuration (kind: tile / slab / stream)."""
+    out = (ctypes.c_int32 * 8)()
+    _check(_lib.sdm_gx_gemm_config_info(int(path), int(config), out), "sdm_gx_gemm_config_info")
+    return {"TI": out[0], "TC": out[1], "KB": out[2], "stages": out[3], "threads": out[4], "smem": out[5],
+            "kind": CONFIG_KINDS.get(out[6], str(out[6])), "consumer_warps": out[7]}
+
+
+def stream_pieces(ntiles: int, C: int, G: int, b: int) -> list[tuple[int, int, int, int]]:
+    """sdm_gx_gemm_stream_piece: the pieces (tile, j0, j1, kind) CTA b of G runs, in order, under the stream
+    kernel's split of a step of ntiles tiles (host code shared with the kernel; no GPU needed)."""
+    out = (ctypes.c_int32 * 4)()
+    n = _lib.sdm_gx_gemm_stream_piece(int(ntiles), int(C), int(G), int(b), -1, out)
+    if n < 0:
+        raise GxGemmError(n, "sdm_gx_gemm_stream_piece")
+    res = []
+    for q in range(n):
+        _check(_lib.sdm_gx_gemm_stream_piece(int(ntiles), int(C), int(G), int(b), q, out), "sdm_gx_gemm_stream_piece")
+        res.append((out[0], out[1], out[2], out[3]))
+    return res
 
 
 def num_configs(path: int) -> int:

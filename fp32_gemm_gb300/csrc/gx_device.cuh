@@ -91,6 +91,54 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global memory into this CTA's
+// shared memory; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 1-D bulk copy of `bytes` from this CTA's shared memory to global memory, committed as its own bulk group; the caller
+// waits for it with bulk_wait_all.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+                 "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+// waits until every bulk group this thread committed has completed (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- flags between CTAs (global memory, GPU scope) ---------------------------------------------------------------------
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
+}
+// orders this thread's view of global memory between the generic proxy (ordinary loads / stores) and the async proxy
+// (bulk copies)
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Bounded wait until the flag holds `want`; false if that took longer than timeout_ns. Polls with relaxed loads;
+// once it matches, an acquire fence orders the caller's later reads after the flag writer's release.
+__device__ __forceinline__ bool wait_flag(const uint32_t *f, uint32_t want, int64_t timeout_ns) {
+    uint64_t t0 = 0;
+    bool timed = false;
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(f)) : "memory");
+        if (v == want) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
+        if (!timed) {
+            t0 = global_timer_ns();
+            timed = true;
+        }
+        __nanosleep(100);
+        if (static_cast<int64_t>(global_timer_ns() - t0) > timeout_ns) return false;
+    }
+}
+
 // ---- packed FP32 FMA ------------------------------------------------------------------------------------------------
 // (c0, c1) = (fma(a0, b0, c0), fma(a1, b1, c1)): one fma.rn.f32x2 instruction, each lane an IEEE fused multiply-add
 // rounded to nearest even with subnormals kept, i.e. bit for bit the same as two fmaf calls; half the issue slots.

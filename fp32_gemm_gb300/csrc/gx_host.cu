@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -213,7 +214,7 @@ struct Launch {
 // j-chain's dependent-FMA latency) for every tile it runs in sequence.
 double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
     const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
-    if (ci.slab) {
+    if (ci.kind == 1) {
         // balanced slabs: every SM gets at most ceil(slabs / SMs), in rounds of four on 16 warps; a partial round of
         // k slabs costs about 1 + 0.9 k slabs (measured: its fixed part does not shrink with k)
         const int64_t per_sm = (tiles + sms - 1) / sms;
@@ -222,6 +223,14 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
         const int64_t rounds = (per_sm + 3) / 4;
         const double rate = 128.0 * (ci.eff / 100.0);
         return eq * ci.TI * ci.TC * C / rate + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
+    }
+    if (ci.kind == 2) {
+        // (tile, j) units split evenly over one CTA per SM; a CTA runs up to two partial pieces besides its whole
+        // tiles, and the hand-off of partial sums costs about one k-block's latency
+        const double units = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
+        const double rate = 128.0 * (ci.eff / 100.0);
+        const double pieces = std::ceil(units / static_cast<double>(C)) + 1.0;
+        return units * ci.TI * ci.TC / rate + pieces * (1500.0 + 8.0 * C) + 2000.0;
     }
     const int64_t per_sm = (tiles + sms - 1) / sms;
     const int64_t a = std::min<int64_t>(occ, per_sm);
@@ -233,20 +242,26 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
 }
 
 // The slab kernel needs whole 32-row slabs (C % 32 == 0) and at most two (chunk, column block) per round of four
-// consecutive slabs (C / 32 >= 3).
-bool config_eligible(const ConfigInfo &ci, int64_t C) {
-    if (!ci.slab) return true;
-    return C % ci.TI == 0 && C / ci.TI >= 3;
+// consecutive slabs (C / 32 >= 3). The stream kernel needs the plan's workspace (ws_bytes at least its size) and at
+// least as many tiles as SMs, so that every CTA's range of (tile, j) units is at least one tile long.
+bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int sms, size_t ws_bytes) {
+    if (ci.kind == 1) return C % ci.TI == 0 && C / ci.TI >= 3;
+    if (ci.kind == 2) {
+        const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+        return tiles >= sms && ws_bytes >= stream_workspace_bytes(sms, ci.TI, ci.TC);
+    }
+    return true;
 }
 
-int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
+int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes) {
     if (forced >= 0) return forced;
     auto tiles_of = [&](const ConfigInfo &ci) {
         return P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
     };
     auto usable = [&](int k) {
         const ConfigInfo &ci = tma_config(k);
-        return d.tma_occ[k] >= 1 && config_eligible(ci, C) && !(ci.slab && !d.slab_ok) && tiles_of(ci) < kTwo31;
+        return d.tma_occ[k] >= 1 && config_eligible(ci, P, C, hd, d.sms, ws_bytes) && !(ci.kind == 1 && !d.slab_ok) &&
+               tiles_of(ci) < kTwo31;
     };
     // Small steps (no tile of 32+ outputs per thread fills the SMs): the step is bound by latency, and the measured
     // best is the configuration with the most tiles that still fit one wave (one tile per SM), i.e. the most
@@ -278,7 +293,7 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     for (int k = 0; k < tma_num_configs(); ++k) {
         if (!usable(k)) continue;
         const ConfigInfo &ci = tma_config(k);
-        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd) * (ci.slab ? 1.0 / 0.95 : 1.0);
+        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd) * (ci.kind == 1 ? 1.0 / 0.95 : 1.0);
         if (est < best * 0.999) {
             best = est;
             bk = k;
@@ -312,7 +327,7 @@ CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t ro
 // Build the launch description for chunks n_first .. n_first + n_count - 1 (pointers and tensor maps originate at
 // n_first). Runs after validate(); makes CUDA calls (device state, descriptor encoding).
 int build_launch(float *du, const float *x, const float *dv, const Shape &sh, int64_t n_first, int64_t n_count,
-                 unsigned flags, Launch *L) {
+                 unsigned flags, Launch *L, void *ws = nullptr, size_t ws_bytes = 0) {
     const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
                            SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL;
     if (flags & ~known) return SDM_GX_E_FLAGS;
@@ -348,24 +363,26 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     int occ = 0;
     if (use_tma) {
         if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
-        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced);
+        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
-        if (!config_eligible(*ci, sh.C) || (ci->slab && !d.slab_ok)) return SDM_GX_E_FLAGS;
+        if (!config_eligible(*ci, sh.P, sh.C, sh.hd, d.sms, ws != nullptr ? ws_bytes : 0) ||
+            (ci->kind == 1 && !d.slab_ok))
+            return SDM_GX_E_FLAGS;
         if (ci->smem > d.optin || d.tma_occ[k] < 1) return SDM_GX_E_SMEM;
-        occ = d.tma_occ[k];
+        occ = ci->kind == 2 ? 1 : d.tma_occ[k];
         l.path = 1;
         l.config = k;
         TmaParams &t = l.tma;
         std::memset(&t, 0, sizeof(t));
         CUresult r;
-        const int du_rows = ci->slab ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
+        const int du_rows = ci->kind == 1 ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
         if ((r = encode_map(&t.tm_x, x0, sh.C, sh.C, n_count, s.x_sj, s.x_sn, ci->TI, ci->KB)) != CUDA_SUCCESS ||
             (r = encode_map(&t.tm_dv, dv0, sh.hd, sh.C, n_count, s.dv_sj, s.dv_sn, ci->TC, ci->KB)) !=
                 CUDA_SUCCESS ||
             (r = encode_map(&t.tm_du, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, du_rows)) !=
                 CUDA_SUCCESS ||
-            (ci->slab &&
+            (ci->kind == 1 &&
              ((r = encode_x_slabs(&t.tm_x4, x0, sh.C, n_count, s.x_sj, s.x_sn, ci->KB)) != CUDA_SUCCESS ||
               (r = encode_map(&t.tm_du1, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, ci->TI)) !=
                   CUDA_SUCCESS)))
@@ -385,6 +402,14 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         t.timeout_ns = (flags & SDM_GX_FLAG_TEST_STALL) ? kStallTestTimeoutNs : kWaitTimeoutNs;
         t.err = d.err;
         t.stall_test = (flags & SDM_GX_FLAG_TEST_STALL) ? 1 : 0;
+        if (ci->kind == 2) {   // workspace: partial sums, flags, control words (sizes as stream_workspace_bytes)
+            unsigned char *w = static_cast<unsigned char *>(ws);
+            const size_t part = (static_cast<size_t>(d.sms) * ci->TI * ci->TC * 4 + 255) / 256 * 256;
+            const size_t fl = (static_cast<size_t>(d.sms) * 4 + 255) / 256 * 256;
+            t.part = reinterpret_cast<float *>(w);
+            t.flags = reinterpret_cast<uint32_t *>(w + part);
+            t.ctl = reinterpret_cast<uint32_t *>(w + part + fl);
+        }
     } else {
         if (forced >= generic_num_configs()) return SDM_GX_E_FLAGS;
         const int k = choose_generic_config(d, sh.P, sh.C, sh.hd, forced);
@@ -414,7 +439,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     if (forced_occ > 0) occ = std::min(occ, forced_occ);
     const int64_t tiles = l.path ? l.tma.ntiles : l.gen.ntiles;
     const int64_t slots = static_cast<int64_t>(d.sms) * occ;
-    l.grid = static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
+    // the stream kernel runs one CTA per SM (its workspace is sized for that grid)
+    l.grid = (ci->kind == 2 && l.path == 1) ? d.sms : static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
     sdm_gx_geom &gm = l.geom;
     gm.path = l.path;
     gm.config = l.config;
@@ -529,16 +555,66 @@ int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, in
     return SDM_GX_OK;
 }
 
-int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
-                            int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max, unsigned flags) {
+int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
+                                    int64_t C, int64_t hd, const sdm_gx_strides *strides, unsigned flags,
+                                    size_t *bytes) {
+    if (bytes == nullptr) return SDM_GX_E_NULL;
+    *bytes = 0;
+    Shape sh;
+    int rc = ex_common(const_cast<float *>(d_u), x, d_dv, 0, N, P, C, hd, strides, &sh);
+    if (rc != SDM_GX_OK) return rc;
+    int dev = 0;
+    const DevState *dsp = nullptr;
+    rc = device_state(&dev, &dsp);
+    if (rc != SDM_GX_OK) return rc;
+    if ((flags & SDM_GX_FLAG_GENERIC) || !tma_eligible(d_u, x, d_dv, sh.s)) return SDM_GX_OK;
+    size_t need = 0;
+    for (int k = 0; k < tma_num_configs(); ++k) {
+        const ConfigInfo &ci = tma_config(k);
+        if (ci.kind != 2 || dsp->tma_occ[k] < 1) continue;
+        const size_t b = stream_workspace_bytes(dsp->sms, ci.TI, ci.TC);
+        if (config_eligible(ci, P, C, hd, dsp->sms, b)) need = std::max(need, b);
+    }
+    *bytes = need;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N,
+                               int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max,
+                               unsigned flags, void *workspace, size_t workspace_bytes) {
     if (out == nullptr) return SDM_GX_E_NULL;
     *out = nullptr;
     Shape sh;
     int rc = ex_common(d_u, x, d_dv, ti_max, N, P, C, hd, strides, &sh);
     if (rc != SDM_GX_OK) return rc;
+    if (workspace != nullptr) {
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SDM_GX_E_ALIGN;
+        const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace);
+        const Span sw{w0, w0 + workspace_bytes};
+        if (overlaps(sw, span_of(d_u, 0, sh.N, sh.s.du_sn, sh.s.du_si, sh.C, sh.hd)) ||
+            overlaps(sw, span_of(x, 0, sh.N, sh.s.x_sn, sh.s.x_sj, sh.C, sh.C)) ||
+            overlaps(sw, span_of(d_dv, 0, sh.N, sh.s.dv_sn, sh.s.dv_sj, sh.C, sh.hd)))
+            return SDM_GX_E_OVERLAP;
+    }
     Launch l;
-    rc = build_launch(d_u, x, d_dv, sh, 0, N, flags, &l);
+    rc = build_launch(d_u, x, d_dv, sh, 0, N, flags, &l, workspace, workspace != nullptr ? workspace_bytes : 0);
     if (rc != SDM_GX_OK) return rc;
+    if (l.path == 1 && tma_config(l.config).kind == 2) {
+        // the workspace must be device memory of this device; its flags and control words start at zero (the
+        // partial sums need no initial value), and the plan's first launch must see that
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, workspace);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SDM_GX_E_DEVICE;
+        }
+        if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != l.device)
+            return SDM_GX_E_DEVICE;
+        unsigned char *ctl0 = reinterpret_cast<unsigned char *>(l.tma.flags);
+        const size_t nctl = 2 * static_cast<size_t>(reinterpret_cast<unsigned char *>(l.tma.ctl) - ctl0);
+        if ((e = cudaMemset(ctl0, 0, nctl)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
+            return fail_cuda(e);
+    }
     sdm_gx_plan *pl = static_cast<sdm_gx_plan *>(std::malloc(sizeof(sdm_gx_plan)));
     if (pl == nullptr) return SDM_GX_E_ALLOC;
     std::memset(static_cast<void *>(pl), 0, sizeof(*pl));
@@ -556,6 +632,11 @@ int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const
     pl->launch = l;
     *out = pl;
     return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
+                            int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max, unsigned flags) {
+    return sdm_gx_gemm_plan_create_ws(out, d_u, x, d_dv, N, P, C, hd, strides, ti_max, flags, nullptr, 0);
 }
 
 int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl) {
@@ -855,6 +936,37 @@ int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]) {
     return SDM_GX_OK;
 }
 
+int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    const ConfigInfo *ci = nullptr;
+    if (path == 1 && config >= 0 && config < tma_num_configs()) ci = &tma_config(config);
+    if (path == 0 && config >= 0 && config < generic_num_configs()) ci = &generic_config(config);
+    if (ci == nullptr) return SDM_GX_E_FLAGS;
+    out[0] = ci->TI;
+    out[1] = ci->TC;
+    out[2] = ci->KB;
+    out[3] = ci->stages;
+    out[4] = ci->threads;
+    out[5] = ci->smem;
+    out[6] = path == 1 ? ci->kind : 0;
+    out[7] = ci->consumer_warps;
+    return SDM_GX_OK;
+}
+
+int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, int32_t q, int32_t out[4]) {
+    if (out == nullptr) return SDM_GX_E_NULL;
+    if (C < 1 || C > 256 || G < 1 || ntiles < G || ntiles >= kTwo31 || b < 0 || b >= G) return SDM_GX_E_RANGE;
+    const Pieces R = cta_pieces(static_cast<int>(ntiles), C, b, G);
+    if (q < 0) return R.count;
+    if (q >= R.count) return SDM_GX_E_RANGE;
+    const Piece pc = piece_at(R, C, q);
+    out[0] = pc.t;
+    out[1] = pc.j0;
+    out[2] = pc.j1;
+    out[3] = pc.kind;
+    return SDM_GX_OK;
+}
+
 int sdm_gx_gemm_num_configs(int32_t path) {
     if (path == 1) return tma_num_configs();
     if (path == 0) return generic_num_configs();
@@ -891,8 +1003,8 @@ const char *sdm_gx_strerror(int status) {
         case SDM_GX_E_NULL: return "a required pointer is NULL";
         case SDM_GX_E_SHAPE: return "need 1 <= C <= 256 and 1 <= hd < 2^20";
         case SDM_GX_E_RANGE: return "step out of range (need 1 <= P <= N < 2^31 and 0 <= ti < N / P)";
-        case SDM_GX_E_ALIGN: return "operands must be 4-byte aligned";
-        case SDM_GX_E_OVERLAP: return "d_u overlaps x or d_dv (the in-place update needs disjoint operands)";
+        case SDM_GX_E_ALIGN: return "operands must be 4-byte aligned (a plan workspace 256-byte aligned)";
+        case SDM_GX_E_OVERLAP: return "d_u overlaps x or d_dv (the in-place update needs disjoint operands), or the workspace overlaps an operand";
         case SDM_GX_E_STRIDE: return "strides do not describe a non-overlapping [N, rows, cols] layout";
         case SDM_GX_E_GRID: return "too many tiles in one step";
         case SDM_GX_E_SMEM: return "shared memory exceeds the device's opt-in limit";

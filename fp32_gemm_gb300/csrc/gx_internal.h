@@ -12,6 +12,7 @@ namespace sdmgx {
 constexpr uint32_t kErrConsumerWait = 1u;   // a consumer warp gave up waiting for a staged k-block or d_u tile
 constexpr uint32_t kErrProducerWait = 2u;   // the producer gave up waiting for a free stage / d_u buffer
 constexpr uint32_t kErrDrainWait = 4u;      // the producer gave up waiting for its own copies after an abort
+constexpr uint32_t kErrHandoffWait = 8u;    // stream kernel: the partial sums of the previous CTA did not appear
 
 // Parameters of the TMA-fed kernel. The tensor maps describe x [n][j][i], d_dv [n][j][c] and d_u [n][i][c] as 3-D
 // float32 tensors (innermost first: i / c, then rows, then chunks). Chunk coordinate of step-local chunk p:
@@ -32,6 +33,11 @@ struct TmaParams {
     int64_t timeout_ns;     // bound of every mbarrier wait
     uint32_t *err;          // the device error word (kErr* bits)
     int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
+    // stream kernel only (the plan's workspace): partial sums [grid][TI][TC] of each CTA's leading piece, one flag
+    // per CTA, and one launch counter (the epoch) per CTA
+    float *part;
+    uint32_t *flags;
+    uint32_t *ctl;
 };
 
 // Parameters of the generic kernel (any strides, 4-byte alignment).
@@ -49,8 +55,60 @@ struct GenericParams {
 struct ConfigInfo {
     int TI, TC, KB, stages, threads, smem, RM, RN, consumer_warps;
     int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
-    int slab;   // 1: the balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3)
+    int kind;   // 0: tile kernel; 1: balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3);
+                // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace)
 };
+
+// Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,
+// one launch counter per CTA (each part 256-byte aligned).
+inline size_t stream_workspace_bytes(int grid, int TI, int TC) {
+    const size_t part = (static_cast<size_t>(grid) * TI * TC * 4 + 255) / 256 * 256;
+    const size_t words = (static_cast<size_t>(grid) * 4 + 255) / 256 * 256;
+    return part + 2 * words;
+}
+
+// The stream kernel's split of one step's work: W = ntiles x C units (tile t, j) in the order (t, j); CTA b of G takes
+// units [b W / G, (b + 1) W / G). With W / G >= C its range is the tail of tile ta (j >= ja, continuing CTA b - 1's
+// partial sums) if ja > 0, whole tiles, and the head of tile tb (j < je, whose partial sums CTA b + 1 continues) if
+// je < C. Host and device share this code (the host exports it for tests).
+struct Piece {
+    int t;        // tile
+    int j0, j1;   // j range [j0, j1)
+    int kind;     // 0: whole tile; 1: head (publishes its partial sums); 2: tail (continues from CTA b - 1's)
+};
+
+struct Pieces {
+    int ta, ja, tb, je;          // range [ta*C + ja, tb*C + je) of units (je in 1..C)
+    int has_head, has_tail, first_full, nfull, count;
+};
+
+__host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G) {
+    const int64_t W = static_cast<int64_t>(ntiles) * C;
+    const int64_t lo = static_cast<int64_t>(b) * W / G;
+    const int64_t hi = static_cast<int64_t>(b + 1) * W / G;
+    Pieces R;
+    R.ta = static_cast<int>(lo / C);
+    R.ja = static_cast<int>(lo - static_cast<int64_t>(R.ta) * C);
+    R.tb = static_cast<int>((hi - 1) / C);
+    R.je = static_cast<int>(hi - static_cast<int64_t>(R.tb) * C);
+    R.has_tail = R.ja > 0 ? 1 : 0;
+    R.has_head = R.je < C ? 1 : 0;
+    R.first_full = R.has_tail ? R.ta + 1 : R.ta;
+    const int last_full = R.has_head ? R.tb - 1 : R.tb;
+    R.nfull = last_full >= R.first_full ? last_full - R.first_full + 1 : 0;
+    R.count = R.has_head + R.nfull + R.has_tail;
+    return R;
+}
+
+// piece q of a CTA, in execution order: head, whole tiles, tail
+__host__ __device__ inline Piece piece_at(const Pieces &R, int C, int q) {
+    if (R.has_head) {
+        if (q == 0) return Piece{R.tb, 0, R.je, 1};
+        --q;
+    }
+    if (q < R.nfull) return Piece{R.first_full + q, 0, C, 0};
+    return Piece{R.ta, R.ja, C, 2};
+}
 
 // TMA path
 int tma_num_configs();

@@ -567,6 +567,315 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
     }
 }
 
+// ---- the stream kernel: the tile kernel with the step's (tile, j) work split evenly over the CTAs ----------------------
+// Every output's chain runs over j = 0..C-1 in order, but nothing requires one CTA to run all of it: a chain stopped
+// after some j and continued later from the same FP32 accumulator value gives the same bits. So the step's work is laid
+// out as W = tiles x C units (tile t, j) in the order (t, j), and CTA b takes units [b W / G, (b + 1) W / G): the SMs
+// get the same work to within one j, where whole tiles leave 104 of 152 SMs with a second tile on the large shape.
+// With W / G >= C (the host's condition) a CTA's range is, in order, the tail of a tile whose leading j belong to CTA
+// b - 1, some whole tiles, and the leading j of a tile whose tail belongs to CTA b + 1 (cta_pieces). It runs them as
+//   1. the head piece first: the first je values of j of its last tile, from +0. The consumer warps leave their
+//      accumulators in the d_u buffer (idle until the first d_u box; fragment order, store_frag) and go on at once;
+//      the publisher warp copies those TI x TC values to the workspace with one bulk store, waits for it, and marks
+//      the CTA's flag with this launch's epoch; the producer issues the CTA's first d_u box only after that;
+//   2. its whole tiles, as in the tile kernel;
+//   3. the tail piece last: the producer waits (bounded) for CTA b - 1's flag, copies that CTA's partial sums into a
+//      shared buffer of their own with one bulk copy, and the consumers continue the chain from them at j = ja, then
+//      add d_u.
+// CTA b - 1 finishes its head piece after ja units of work; CTA b starts its tail after (W / G) - (C - ja) >= ja units,
+// so the hand-off is normally ready long before it is needed. Flags carry an epoch: each CTA counts the launches that
+// used the workspace in its own control word, which its publisher warp reads and advances right after the
+// grid-dependency wait (the next launch reads it only after this one has completed; every CTA of every launch counts,
+// so all CTAs agree on the epoch). A flag left by an earlier launch, or by an aborted one, therefore never matches.
+template <class T, int EFF_>
+struct KCfg : T {
+    static constexpr int SLAB = 2;
+    static constexpr int EFF = EFF_;
+    static constexpr int THREADS = (T::NCW + 2) * 32;         // consumers, producer, publisher
+    static constexpr int OFF_P = T::OFF_BAR;                  // the incoming partial sums [TI][TC]
+    static constexpr int OFF_BAR = OFF_P + T::DU_BYTES;
+    // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
+    static constexpr int NBAR = 2 * T::ST + 6;
+    static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
+    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8 + 4, 128) + 128;
+    static_assert((T::TI * T::TC * 4) % 16 == 0, "the partial-sum tile is copied in 16-byte units");
+};
+
+// A consumer thread's accumulators, kept in their own fragment order instead of the tile's row-major order: vector v
+// (v = sr * RN + c) of thread tid holds rows sr*4 .. sr*4 + 3 of the thread's column c, and sits at float offset
+// (v * NCW*32 + tid) * 4. Column runs of four rows match the register pairs of the packed FMA (rows r, r + 1), and a
+// warp's 16-byte accesses to one v are 512 contiguous bytes (no bank conflicts). Both ends of a hand-off use the same
+// thread mapping, so the partial sums never need the tile's own layout.
+template <class Cfg>
+__device__ __forceinline__ void store_frag(float *dst, int tid, const float (&acc)[Cfg::RM][Cfg::RN]) {
+    static_assert(Cfg::RM % 4 == 0, "fragments are column runs of four rows");
+#pragma unroll
+    for (int sr = 0; sr < Cfg::RM / 4; ++sr) {
+#pragma unroll
+        for (int c = 0; c < Cfg::RN; ++c) {
+            const float v4[4] = {acc[sr * 4][c], acc[sr * 4 + 1][c], acc[sr * 4 + 2][c], acc[sr * 4 + 3][c]};
+            dev::Vec<4>::store(dst + ((sr * Cfg::RN + c) * Cfg::NCW * 32 + tid) * 4, v4);
+        }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void load_frag(const float *src, int tid, float (&acc)[Cfg::RM][Cfg::RN]) {
+#pragma unroll
+    for (int sr = 0; sr < Cfg::RM / 4; ++sr) {
+#pragma unroll
+        for (int c = 0; c < Cfg::RN; ++c) {
+            float v4[4];
+            dev::Vec<4>::load(src + ((sr * Cfg::RN + c) * Cfg::NCW * 32 + tid) * 4, v4);
+            acc[sr * 4][c] = v4[0];
+            acc[sr * 4 + 1][c] = v4[1];
+            acc[sr * 4 + 2][c] = v4[2];
+            acc[sr * 4 + 3][c] = v4[3];
+        }
+    }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1) gx_stream_kernel(const __grid_constant__ TmaParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_s = dev::smem_addr(smem_raw);
+    const uint32_t base_s = (raw_s + 127u) & ~127u;
+    unsigned char *const base_g = smem_raw + (base_s - raw_s);
+    const uint32_t bar0 = base_s + Cfg::OFF_BAR;
+    const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
+    const uint32_t du_empty = du_full + 8u;
+    const uint32_t part_full = du_empty + 8u;
+    const uint32_t head_staged = part_full + 8u;   // NCW arrivals: the head's accumulators are in the d_u buffer
+    const uint32_t head_stored = head_staged + 8u; // 1 arrival: the publisher's bulk store has read them
+    const uint32_t epoch_known = head_stored + 8u; // 1 arrival: the publisher has put the epoch in shared memory
+    volatile uint32_t *const epoch_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_EPOCH);
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    const int b = static_cast<int>(blockIdx.x);
+    const int G = static_cast<int>(gridDim.x);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::ST; ++s) {
+            dev::mbar_init(bar0 + 8u * s, 1);
+            dev::mbar_init(bar0 + 8u * (Cfg::ST + s), Cfg::NCW);
+        }
+        dev::mbar_init(du_full, 1);
+        dev::mbar_init(du_empty, Cfg::NCW);
+        dev::mbar_init(part_full, 1);
+        dev::mbar_init(head_staged, Cfg::NCW);
+        dev::mbar_init(head_stored, 1);
+        dev::mbar_init(epoch_known, 1);
+        dev::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const Pieces R = cta_pieces(p.ntiles, p.C, b, G);
+
+    if (warp == Cfg::NCW + 1) {
+        // ------------------------------------------------ publisher -----------------------------------------------
+        if (lane != 0) return;
+        dev::grid_dependency_wait();
+        // this launch's epoch: the CTA's count of earlier launches, advanced at once (nothing else reads the word)
+        const uint32_t epoch = *reinterpret_cast<volatile const uint32_t *>(p.ctl + b);
+        *reinterpret_cast<volatile uint32_t *>(p.ctl + b) = epoch + 1u;
+        *epoch_s = epoch;
+        dev::mbar_arrive(epoch_known);
+        if (R.has_head) {
+            if (dev::mbar_wait(head_staged, 0u, p.timeout_ns)) {
+                dev::bulk_store(p.part + static_cast<int64_t>(b) * Cfg::TI * Cfg::TC, base_s + Cfg::OFF_U,
+                                Cfg::DU_TX);
+                dev::bulk_wait_all();
+                dev::fence_proxy_async_global();
+                dev::st_release_gpu(p.flags + b, epoch + 1u);
+            } else {
+                atomicOr(p.err, kErrConsumerWait);
+            }
+            dev::mbar_arrive(head_stored);   // the d_u buffer is free again (also after a failed wait: no copy ran)
+        }
+        return;
+    }
+
+    if (warp == Cfg::NCW) {
+        // ------------------------------------------------ producer ------------------------------------------------
+        if (lane != 0) return;
+        int it = 0;            // stage iterations issued (over all pieces)
+        int du_issued = 0;     // d_u boxes issued
+        int npre = 0;          // stages of piece 0 whose x box went out before the dependency wait
+        bool du0_early = false;
+        bool part_issued = false;
+        bool ok = true;
+        uint32_t err_bit = kErrProducerWait;
+        {
+            dev::prefetch_tensormap(&p.tm_x);
+            dev::prefetch_tensormap(&p.tm_dv);
+            dev::prefetch_tensormap(&p.tm_du);
+            const Piece P0 = piece_at(R, p.C, 0);
+            const Tile tl = decode_tile<Cfg>(p, P0.t);
+            const int nkb0 = (P0.j1 - P0.j0 + Cfg::KB - 1) / Cfg::KB;
+            npre = nkb0 < Cfg::ST ? nkb0 : Cfg::ST;
+            for (int s = 0; s < npre; ++s) {
+                dev::mbar_arrive_expect_tx(bar0 + 8u * s, Cfg::STAGE_TX);
+                if (s == 0 && p.stall_test) continue;   // test hook: stage 0 never completes
+                dev::tma_load_3d(base_s + s * Cfg::XS_BYTES, &p.tm_x, tl.i0, P0.j0 + s * Cfg::KB, tl.n, bar0 + 8u * s);
+            }
+            if (p.prefetch) {
+                for (int kb = 0; kb < nkb0; ++kb) dev::tma_prefetch_3d(&p.tm_dv, tl.c0, P0.j0 + kb * Cfg::KB, tl.n);
+            }
+            if (P0.kind == 0) {   // d_u of a whole first tile: read before the wait (the caller's PDL contract)
+                dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
+                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+                du_issued = 1;
+                du0_early = true;
+            }
+        }
+        dev::grid_dependency_wait();
+        dev::launch_dependents();
+        for (int q = 0; q < R.count && ok; ++q) {
+            const Piece P = piece_at(R, p.C, q);
+            const Tile tl = decode_tile<Cfg>(p, P.t);
+            if (P.kind == 2) {
+                // the partial sums of CTA b - 1 (its head piece: this tile's j < ja)
+                if (!dev::mbar_wait(epoch_known, 0u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (!dev::wait_flag(p.flags + (b - 1), *epoch_s + 1u, p.timeout_ns)) {
+                    ok = false;
+                    err_bit = kErrHandoffWait;
+                    break;
+                }
+                dev::fence_proxy_async_global();
+                dev::mbar_arrive_expect_tx(part_full, Cfg::DU_TX);
+                dev::bulk_load(base_s + Cfg::OFF_P, p.part + static_cast<int64_t>(b - 1) * Cfg::TI * Cfg::TC,
+                               Cfg::DU_TX, part_full);
+                part_issued = true;
+            }
+            const int nkb = (P.j1 - P.j0 + Cfg::KB - 1) / Cfg::KB;
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % Cfg::ST;
+                const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+                const uint32_t full = bar0 + 8u * s;
+                const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
+                const int j = P.j0 + kb * Cfg::KB;
+                if (it < npre) {   // armed, x already in flight: add the d_dv box
+                    if (!(it == 0 && p.stall_test)) dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, j, tl.n, full);
+                    continue;
+                }
+                if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(full, Cfg::STAGE_TX);
+                dev::tma_load_3d(base_s + s * Cfg::XS_BYTES, &p.tm_x, tl.i0, j, tl.n, full);
+                dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, j, tl.n, full);
+            }
+            if (!ok) break;
+            // d_u of a piece that ends its tile, after the piece's k-blocks (as in the tile kernel). The first box
+            // waits until the publisher has stored the head's partial sums out of the d_u buffer.
+            if (P.kind != 1 && !(q == 0 && du0_early)) {
+                const bool waited = du_issued > 0
+                                        ? dev::mbar_wait(du_empty, static_cast<uint32_t>(du_issued - 1) & 1u,
+                                                         p.timeout_ns)
+                                        : (!R.has_head || dev::mbar_wait(head_stored, 0u, p.timeout_ns));
+                if (!waited) {
+                    ok = false;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
+                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+                ++du_issued;
+            }
+        }
+        if (p.stall_test) ok = false;   // the test hook always unwinds: its consumers never took every stage
+        if (!ok) {
+            atomicOr(p.err, err_bit);
+            // Unwind as the tile kernel does: wait for the copies this thread issued before leaving.
+            const int lo = it - Cfg::ST > 0 ? it - Cfg::ST : 0;
+            for (int k = lo; k < it; ++k) {
+                if (!dev::mbar_wait(bar0 + 8u * (k % Cfg::ST), static_cast<uint32_t>(k / Cfg::ST) & 1u, p.timeout_ns))
+                    atomicOr(p.err, kErrDrainWait);
+            }
+            if (du_issued > 0 && !dev::mbar_wait(du_full, static_cast<uint32_t>(du_issued - 1) & 1u, p.timeout_ns))
+                atomicOr(p.err, kErrDrainWait);
+            if (part_issued && !dev::mbar_wait(part_full, 0u, p.timeout_ns)) atomicOr(p.err, kErrDrainWait);
+        }
+        return;
+    }
+
+    // -------------------------------------------------- consumers --------------------------------------------------
+    const int wm = warp % Cfg::WM;
+    const int wn = warp / Cfg::WM;
+    const int lm = lane / Cfg::LN;
+    const int ln = lane % Cfg::LN;
+    int ro[Cfg::SR], co[Cfg::SN];
+#pragma unroll
+    for (int s = 0; s < Cfg::SR; ++s) ro[s] = wm * Cfg::RM * Cfg::LM + s * Cfg::VR * Cfg::LM + lm * Cfg::VR;
+#pragma unroll
+    for (int s = 0; s < Cfg::SN; ++s) co[s] = wn * Cfg::RN * Cfg::LN + s * Cfg::VN * Cfg::LN + ln * Cfg::VN;
+
+    dev::grid_dependency_wait();   // the workspace and d_u are touched only after the predecessor grid has completed
+    float *const us = reinterpret_cast<float *>(base_g + Cfg::OFF_U);
+    const float *const ps = reinterpret_cast<const float *>(base_g + Cfg::OFF_P);
+    int it = 0;
+    int du_used = 0;
+    bool failed = false;
+    for (int q = 0; q < R.count && !failed; ++q) {
+        const Piece P = piece_at(R, p.C, q);
+        const Tile tl = decode_tile<Cfg>(p, P.t);
+        float acc[Cfg::RM][Cfg::RN];
+        if (P.kind == 2) {
+            if (!__all_sync(0xffffffffu, dev::mbar_wait(part_full, 0u, p.timeout_ns))) {
+                failed = true;
+                break;
+            }
+            load_frag<Cfg>(ps, static_cast<int>(threadIdx.x), acc);
+        } else {
+#pragma unroll
+            for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+                for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = 0.0f;   // +0: the chain's start value
+            }
+        }
+        const int nkb = (P.j1 - P.j0 + Cfg::KB - 1) / Cfg::KB;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const int s = it % Cfg::ST;
+            const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
+            if (!__all_sync(0xffffffffu, dev::mbar_wait(bar0 + 8u * s, ph, p.timeout_ns))) {
+                failed = true;
+                break;
+            }
+            const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
+            const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
+            const int nj = P.j1 - (P.j0 + kb * Cfg::KB);
+            if (nj >= Cfg::KB) {
+                chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+            } else {
+                chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+        }
+        if (failed) break;
+        if (P.kind == 1) {
+            // the head's accumulators into the (still idle) d_u buffer, visible to the publisher's bulk store
+            store_frag<Cfg>(us, static_cast<int>(threadIdx.x), acc);
+            dev::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(head_staged);
+            continue;
+        }
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
+            failed = true;
+            break;
+        }
+        epilogue<Cfg>(p, tl, us, ro, co, acc);
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(du_empty);
+        ++du_used;
+    }
+    if (failed && lane == 0) atomicOr(p.err, kErrConsumerWait);
+}
+
 template <class Cfg>
 cudaError_t launch_cfg(const TmaParams &p, int grid, cudaStream_t st, int pdl) {
     cudaLaunchConfig_t cfg = {};
@@ -581,6 +890,8 @@ cudaError_t launch_cfg(const TmaParams &p, int grid, cudaStream_t st, int pdl) {
     cfg.numAttrs = pdl ? 1 : 0;
     if constexpr (Cfg::SLAB == 1) {
         return cudaLaunchKernelEx(&cfg, gx_slab_kernel<Cfg>, p);
+    } else if constexpr (Cfg::SLAB == 2) {
+        return cudaLaunchKernelEx(&cfg, gx_stream_kernel<Cfg>, p);
     } else {
         return cudaLaunchKernelEx(&cfg, gx_tma_kernel<Cfg>, p);
     }
@@ -590,6 +901,8 @@ template <class Cfg>
 const void *kernel_of() {
     if constexpr (Cfg::SLAB == 1) {
         return reinterpret_cast<const void *>(&gx_slab_kernel<Cfg>);
+    } else if constexpr (Cfg::SLAB == 2) {
+        return reinterpret_cast<const void *>(&gx_stream_kernel<Cfg>);
     } else {
         return reinterpret_cast<const void *>(&gx_tma_kernel<Cfg>);
     }
@@ -617,6 +930,7 @@ using C8 = TCfg<2, 4, 2, 2, 32, 2, 4, 28>;   //  16 x  64,  4 warps
 using C9 = TCfg<4, 4, 1, 1, 32, 2, 8, 25>;   //  16 x  32,  1 warp
 using C10 = TCfg<2, 4, 1, 1, 32, 2, 8, 20>;  //   8 x  32,  1 warp
 using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 warps (rounds of four slabs)
+using C12 = KCfg<C0, 72>;                     // C0's tile with the (tile, j) work split evenly over the CTAs
 
 struct Entry {
     ConfigInfo info;
@@ -627,7 +941,7 @@ struct Entry {
 #define SDMGX_ENTRY(C) Entry{info_of<C>(), kernel_of<C>(), &launch_cfg<C>}
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
-                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11)};
+                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12)};
 #undef SDMGX_ENTRY
 
 }  // namespace

@@ -17,7 +17,8 @@
  * strided entry points take element strides instead (innermost stride always 1).
  *
  * Ownership: the caller owns every device buffer and stream. The library never allocates or frees device memory.
- * A plan holds raw device pointers and host memory only; it is valid while the buffers it names live.
+ * A plan holds raw device pointers and host memory only; it is valid while the buffers it names live. A plan created
+ * with a workspace (sdm_gx_gemm_plan_create_ws) uses that caller-owned device buffer as scratch for as long as it lives.
  *
  * Errors: every entry point returns 0 (SDM_GX_OK) or a negative sdm_gx_status. All argument checks run before any
  * CUDA call. An empty step (nothing to compute) returns 0 without a launch. Calls are asynchronous and
@@ -35,6 +36,7 @@
 #ifndef SDM_GX_GEMM_H_
 #define SDM_GX_GEMM_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -55,8 +57,9 @@ typedef enum sdm_gx_status {
     SDM_GX_E_NULL = -1,          /* a required pointer argument is NULL                                          */
     SDM_GX_E_SHAPE = -2,         /* C outside [1, 256] or hd outside [1, 2^20)                                   */
     SDM_GX_E_RANGE = -3,         /* not 1 <= P <= N < 2^31, or not 0 <= ti < N / P (checked by division)        */
-    SDM_GX_E_ALIGN = -4,         /* an operand pointer is not 4-byte aligned                                     */
-    SDM_GX_E_OVERLAP = -5,       /* d_u overlaps x or d_dv (the in-place update needs disjoint operands)         */
+    SDM_GX_E_ALIGN = -4,         /* an operand pointer is not 4-byte aligned (a plan workspace: 256-byte)        */
+    SDM_GX_E_OVERLAP = -5,       /* d_u overlaps x or d_dv (the in-place update needs disjoint operands), or a
+                                    plan workspace overlaps an operand                                          */
     SDM_GX_E_STRIDE = -6,        /* strides do not describe a non-overlapping [N, rows, cols] layout, or overflow */
     SDM_GX_E_GRID = -7,          /* more than 2^31 - 1 tiles in one step                                         */
     SDM_GX_E_SMEM = -8,          /* the kernel's shared memory exceeds the device's opt-in limit                 */
@@ -143,6 +146,32 @@ SDM_GX_API int sdm_gx_gemm_geometry(const float *d_u, const float *x, const floa
 SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P,
                             int64_t C, int64_t hd, const sdm_gx_strides *strides, int64_t ti_max, unsigned flags);
 
+/*
+ * A plan with a workspace. With a large enough workspace the plan may pick the stream kernel: the step's work, in
+ * units of (tile, j), split evenly over one CTA per SM instead of in whole tiles. A CTA then runs the first j of one
+ * tile and another CTA continues those outputs' chains from the FP32 accumulators that the first one left in the
+ * workspace. Each output still gets the one fixed chain acc = fmaf(x, d_dv, acc) for j = 0..C-1 from +0 and the one
+ * final add, so the results are bit for bit those of every other kernel. The pages split work only in whole chunks;
+ * this split is ours, for SM balance (e.g. 256 tiles on 152 SMs).
+ *   workspace: device memory of the current device, 256-byte aligned, not overlapping d_u, x or d_dv, at least
+ *   sdm_gx_gemm_plan_workspace_size() bytes; NULL (or too small) gives the plan of sdm_gx_gemm_plan_create.
+ *   The call zero-fills the workspace's control words and waits for that (a device synchronisation).
+ *   The workspace belongs to the plan until it is destroyed: no other plan may use it, and the steps of this plan
+ *   must run one after the other (stream-ordered, as sdm_gx_gemm_plan_run, the graph and the host driver launch
+ *   them; with PDL each step touches the workspace only after its grid-dependency wait). Steps of one plan running
+ *   concurrently on unordered streams would race on it.
+ * Errors as sdm_gx_gemm_plan_create, plus SDM_GX_E_ALIGN / SDM_GX_E_OVERLAP / SDM_GX_E_DEVICE for the workspace.
+ */
+SDM_GX_API int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N,
+                                          int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides,
+                                          int64_t ti_max, unsigned flags, void *workspace, size_t workspace_bytes);
+
+/* Bytes of workspace that lets a plan of this shape and layout use the stream kernel on the current device (0: no
+ * kernel of this shape uses one). About (number of SMs) x TI x TC x 4 bytes: 9.5 MiB for 128 x 128 tiles on 152 SMs. */
+SDM_GX_API int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const float *d_dv, int64_t N,
+                                               int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides,
+                                               unsigned flags, size_t *bytes);
+
 /* Launch step ti of a plan on `stream` (pdl as above). Errors: SDM_GX_E_PLAN (NULL / corrupt plan),
  * SDM_GX_E_PLAN_TI (ti < 0 or ti > ti_max), SDM_GX_E_PLAN_DEVICE (current device differs), SDM_GX_E_CUDA. */
 SDM_GX_API int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl);
@@ -216,12 +245,27 @@ SDM_GX_API int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int
  * path 0 = generic (config 0..2 = 16/32/64 rows), path 1 = TMA (config index as in sdm_gx_geom). out[4]. */
 SDM_GX_API int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]);
 
+/* Static description of configuration `config` of a path (for sweeps and tests): out[0..7] = TI, TC, KB, stages,
+ * threads per CTA, dynamic shared memory bytes, kind (0: tile kernel, 1: balanced slab kernel, 2: stream kernel, which
+ * needs a plan workspace), consumer warps. SDM_GX_E_FLAGS for an unknown path or index. */
+SDM_GX_API int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]);
+
+/* The stream kernel's split of a step (host code shared with the kernel, for tests and tools): the step's
+ * ntiles x C units (tile t, j), ordered by (t, j), go to CTAs 0..G-1 in equal contiguous ranges (CTA b: units
+ * [b W / G, (b + 1) W / G), W = ntiles x C). Needs 1 <= C <= 256 and 1 <= G <= ntiles < 2^31 (every range is then at
+ * least one tile long), 0 <= b < G. With q < 0 it returns the number of pieces CTA b runs; otherwise it writes piece q
+ * (in the order the CTA runs them) to out[0..3] = tile, j0, j1 (the piece covers j0 <= j < j1) and kind (0: a whole
+ * tile; 1: the head of a tile, run first, whose accumulators CTA b + 1 continues; 2: the tail of a tile, run last,
+ * continuing CTA b - 1's accumulators) and returns 0. SDM_GX_E_RANGE for arguments outside those bounds. */
+SDM_GX_API int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, int32_t q, int32_t out[4]);
+
 /* Number of tile configurations of a path (for sweeps and tests). */
 SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
 
 /* The device error word of the current device: nonzero bits mean a kernel gave up a bounded wait (bit 0: a consumer
  * waited too long for staged data, bit 1: the producer waited too long for a free stage, bit 2: a drain wait gave
- * up). Synchronizes the device. clear != 0 resets it to 0 afterwards. */
+ * up, bit 3: the stream kernel waited too long for another CTA's partial sums). Synchronizes the device. clear != 0
+ * resets it to 0 afterwards. */
 SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
 
 /* Launches of the library's kernels since load: out[0] = step kernels, out[1] = producer kernels,

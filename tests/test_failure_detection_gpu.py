@@ -37,3 +37,31 @@ def test_expired_waits_are_reported_and_the_context_survives():
     assert_bitwise(du2.host(), want, "after the stall test")
     assert gx.device_error(clear=True) == 0
     assert np.isfinite(du2.host()).all()
+
+
+def test_stream_kernel_expired_waits_are_reported():
+    """The same hook on the stream kernel (one CTA per SM, chains handed between CTAs through the plan's workspace):
+    both stalled launches complete with the error word set, the context stays usable, and a stream-kernel plan on
+    fresh buffers then matches the oracle over two passes of its steps."""
+    k = [c for c in range(gx.num_configs(1)) if gx.config_info(1, c)["kind"] == "stream"][0]
+    w = synth.Workload("stall_stream", 71, T=2, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    du, dx, dv = (DevArray(inp[k_]) for k_ in ("d_u", "x", "d_dv"))
+    gx.device_error(clear=True)
+    stalled = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.FLAG_TEST_STALL | gx.config_flag(k))
+    assert stalled.geometry()["config"] == k
+    stalled.step(0)
+    stalled.step(1)
+    torch.cuda.synchronize()
+    word = gx.device_error(clear=True)
+    assert word & 1, f"consumer wait not reported: {word:#x}"
+    du2, dx2, dv2 = (DevArray(inp[k_]) for k_ in ("d_u", "x", "d_dv"))
+    ok = gx.Plan(du2.t, dx2.t, dv2.t, w.P, flags=gx.config_flag(k))
+    ok.run(pdl=True)
+    ok.run(pdl=True)
+    torch.cuda.synchronize()
+    want = inp["d_u"].copy()
+    oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
+    oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
+    assert_bitwise(du2.host(), want, "stream kernel after the stall test")
+    assert gx.device_error(clear=True) == 0

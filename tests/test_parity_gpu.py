@@ -79,16 +79,26 @@ def test_every_tma_config_ragged(config):
     if config >= gx.num_configs(1):
         pytest.skip("no such configuration")
     w = _ragged_workload()
-    if gx.kernel_attrs(1, config)["max_threads"] == 544 and config == gx.num_configs(1) - 1:
+    kind = gx.config_info(1, config)["kind"]
+    if kind == "slab":
         # the slab kernel needs whole 32-row slabs: ragged in columns and P only
         w = synth.Workload("ragged_slab", 65, T=2, P=5, C=96, hd=76, x_scale="inv_sqrt_c")
+    elif kind == "stream":
+        # the stream kernel needs at least one tile per SM: 160 one-tile chunks, ragged in rows and columns
+        w = synth.Workload("ragged_stream", 67, T=2, P=160, C=100, hd=76, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, w.P, [1, 0])
     du, dx, dv = _dev(inp)
     flags = gx.config_flag(config)
-    g = gx.geometry(du.t, dx.t, dv.t, w.P, flags=flags)
-    assert g["path"] == 1 and g["config"] == config
+    if kind == "stream":   # stateless calls have no workspace: the stream kernel exists for plans only
+        with pytest.raises(gx.GxGemmError) as e:
+            gx.geometry(du.t, dx.t, dv.t, w.P, flags=flags)
+        assert e.value.name == "SDM_GX_E_FLAGS"
+    else:
+        g = gx.geometry(du.t, dx.t, dv.t, w.P, flags=flags)
+        assert g["path"] == 1 and g["config"] == config
     pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=flags)
+    assert pl.geometry()["config"] == config
     pl.run(1, -1, pdl=True)
     torch.cuda.synchronize()
     assert_bitwise(du.host(), want, f"tma config {config}")
@@ -176,12 +186,15 @@ def test_large_two_steps():
     w = synth.WORKLOADS["large"]
     inp = synth.make_inputs(w, N=2 * w.P)
     want, _ = _oracle_steps(inp, w.P, [0, 1])
-    du, dx, dv = _dev(inp)
-    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
-    pl.run(pdl=True)
-    torch.cuda.synchronize()
-    assert_bitwise(du.host(), want, "large 2 steps")
-    assert du.guards_intact()
+    for workspace in (True, False):   # the plan's choice with a workspace (stream kernel) and without (tile kernel)
+        du, dx, dv = _dev(inp)
+        pl = gx.Plan(du.t, dx.t, dv.t, w.P, workspace=workspace)
+        kind = gx.config_info(1, pl.geometry()["config"])["kind"]
+        assert (kind == "stream") == workspace, kind
+        pl.run(pdl=True)
+        torch.cuda.synchronize()
+        assert_bitwise(du.host(), want, f"large 2 steps ({kind} kernel)")
+        assert du.guards_intact()
 
 
 def test_kernel_attrs_no_spills():
@@ -375,7 +388,7 @@ def test_x_and_d_dv_may_alias():
 def test_slab_kernel_shapes(P, C, hd, T):
     """The balanced slab kernel: full rounds (four slabs of one chunk), rounds across chunks, partial rounds, several
     column blocks, fewer slabs than SMs."""
-    slab = gx.num_configs(1) - 1
+    slab = [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "slab"][0]
     w = synth.Workload("slab", 66, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, P, range(T))
@@ -405,3 +418,87 @@ def test_run_host_overlapped_copies():
     torch.cuda.synchronize()
     assert_bitwise(host["d_u"].numpy(), want, "run_host x2")
     assert_bitwise(host["x"].numpy(), inp["x"], "x host unchanged")
+
+
+def _stream_config():
+    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "stream"][0]
+
+
+@pytest.mark.parametrize("P,C,hd,T", [(160, 100, 76, 2), (153, 64, 64, 2), (100, 128, 200, 2), (304, 128, 128, 2),
+                                      (200, 32, 500, 2), (256, 128, 128, 2)])
+def test_stream_kernel_shapes(P, C, hd, T):
+    """The stream kernel (a step's (tile, j) work split evenly over one CTA per SM; chains continued across CTAs from
+    the accumulators left in the plan's workspace): ragged rows and columns, one tile more than SMs (hand-offs with
+    almost no slack), several column blocks, exactly two tiles per CTA (no split), the large step. The chain is
+    captured into a graph and replayed twice, so the workspace's launch epoch advances over 2T launches."""
+    k = _stream_config()
+    w = synth.Workload("stream", 68, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, list(range(T - 1, -1, -1)) * 2)
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(k))
+    g = pl.geometry()
+    assert g["config"] == k and g["ctas"] == g["sms"]
+    assert pl.workspace_bytes > 0
+    gr = pl.graph(T - 1, -1, pdl=True)
+    gr.launch()
+    gr.launch()
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"stream P={P} C={C} hd={hd}")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, "stream")
+    gr.close()
+
+
+def test_stream_kernel_direct_launches_then_graph():
+    """Plan launches outside a graph (plain and PDL) and a graph on the same workspace, interleaved: every launch
+    reads the epoch its predecessor left."""
+    k = _stream_config()
+    w = synth.Workload("stream2", 69, T=3, P=160, C=96, hd=96, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [0, 1, 2, 2, 1, 0, 1])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+    pl.step(0, pdl=False)
+    pl.run(1, 3, pdl=True)
+    gr = pl.graph(2, -1, pdl=True)
+    gr.launch()
+    pl.step(1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "stream interleaved launches")
+    gr.close()
+
+
+def test_stream_workspace_rules():
+    """Without a workspace the stream kernel is not available (forcing it is an error); the workspace size is 0 for
+    shapes with fewer tiles than SMs; a misaligned or overlapping workspace is refused."""
+    k = _stream_config()
+    small = synth.WORKLOADS["tiny"]
+    inp = synth.make_inputs(small)
+    du, dx, dv = _dev(inp)
+    assert gx.workspace_size(du.t, dx.t, dv.t, small.P) == 0
+    w = synth.Workload("stream3", 70, T=1, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    du, dx, dv = _dev(inp)
+    n = gx.workspace_size(du.t, dx.t, dv.t, w.P)
+    assert n > 0
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k), workspace=False)
+    assert e.value.name == "SDM_GX_E_FLAGS"
+    L = gx.lib()
+    import ctypes
+    uv, xv, vv = du.t, dx.t, dv.t
+    s = gx.Strides(xv.stride(0), xv.stride(1), vv.stride(0), vv.stride(1), uv.stride(0), uv.stride(1))
+    buf = torch.empty(n + 512, dtype=torch.uint8, device="cuda")
+    base = (buf.data_ptr() + 255) // 256 * 256
+    h = ctypes.c_void_p()
+    rc = L.sdm_gx_gemm_plan_create_ws(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), w.N, w.P, w.C,
+                                      w.hd, ctypes.byref(s), 0, 0, base + 16, n)
+    assert gx.strerror(rc) and rc == -4          # SDM_GX_E_ALIGN
+    rc = L.sdm_gx_gemm_plan_create_ws(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), w.N, w.P, w.C,
+                                      w.hd, ctypes.byref(s), 0, 0, (uv.data_ptr() + 255) // 256 * 256, n)
+    assert rc == -5                              # SDM_GX_E_OVERLAP
+    rc = L.sdm_gx_gemm_plan_create_ws(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), w.N, w.P, w.C,
+                                      w.hd, ctypes.byref(s), 0, 0, base, n)
+    assert rc == 0
+    L.sdm_gx_gemm_plan_destroy(h)
