@@ -57,6 +57,8 @@ class GxGemmError(RuntimeError):
 SIGNATURES = {
     # name: (restype, argtypes)
     "sdm_gx_gemm_step": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 + [ctypes.c_void_p, ctypes.c_int]),
+    "sdm_gx_gemm_step_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
+                                 [ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_step_ex": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 5 +
                             [ctypes.POINTER(Strides), ctypes.c_void_p, ctypes.c_int, ctypes.c_uint]),
     "sdm_gx_gemm_geometry": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
@@ -166,6 +168,17 @@ def step(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, stream=None) -> None:
     hd = int(d_u.shape[-1])
     _check(_lib.sdm_gx_gemm_step(d_u.data_ptr(), x.data_ptr(), d_dv.data_ptr(), int(ti), int(P), C, hd,
                                  _stream(stream), int(bool(pdl))), "sdm_gx_gemm_step")
+
+
+def step_noalloc(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, stream=None) -> None:
+    """sdm_gx_gemm_step_noalloc: one step like step(), with the library's static scratch as the stream kernel's
+    workspace (allocates nothing; calls on one device must not overlap in time)."""
+    if not (d_u.is_contiguous() and x.is_contiguous() and d_dv.is_contiguous()):
+        raise ValueError("gx_gemm.step_noalloc: contiguous operands")
+    C = int(x.shape[1])
+    hd = int(d_u.shape[-1])
+    _check(_lib.sdm_gx_gemm_step_noalloc(d_u.data_ptr(), x.data_ptr(), d_dv.data_ptr(), int(ti), int(P), C, hd,
+                                         _stream(stream), int(bool(pdl))), "sdm_gx_gemm_step_noalloc")
 
 
 def step_ex(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, flags: int = 0, stream=None) -> None:

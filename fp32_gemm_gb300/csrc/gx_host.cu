@@ -899,6 +899,69 @@ void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan) {
     std::free(plan);
 }
 
+}  // extern "C"
+
+// ---- the entry point that allocates nothing --------------------------------------------------------------------------
+// Its scratch is one static device array per device (each device's module instance has its own copy), used as the
+// stream kernel's workspace: partial sums for up to kNoAllocMaxSms CTAs of 128 x 128 tiles, then flags, then launch
+// counters, laid out as stream_workspace_bytes describes. No call allocates; every call shares the array.
+namespace {
+constexpr int kNoAllocMaxSms = 160;
+constexpr size_t kNoAllocWords = (static_cast<size_t>(kNoAllocMaxSms) * 4 + 255) / 256 * 256;
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(kNoAllocMaxSms) * 128 * 128 * 4 + 2 * kNoAllocWords;
+static __device__ __align__(256) unsigned char g_sdm_gx_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocState {
+    bool init = false;
+    void *scratch = nullptr;
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// once per device, under the lock: the array's device address, and its flags and launch counters set to zero (a
+// memset of existing memory, then a device synchronisation so that every stream sees it)
+int noalloc_scratch(int dev, void **out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocState &st = g_noalloc[dev];
+    if (!st.init) {
+        void *a = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&a, g_sdm_gx_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e);
+        unsigned char *ctl = static_cast<unsigned char *>(a) + kNoAllocScratchBytes - 2 * kNoAllocWords;
+        if ((e = cudaMemset(ctl, 0, 2 * kNoAllocWords)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
+            return fail_cuda(e);
+        st.scratch = a;
+        st.init = true;
+    }
+    *out = st.scratch;
+    return SDM_GX_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int sdm_gx_gemm_step_noalloc(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t P, int64_t C,
+                             int64_t hd, cudaStream_t stream, int pdl) {
+    if (d_u == nullptr || x == nullptr || d_dv == nullptr) return SDM_GX_E_NULL;
+    if (C < 1 || C > 256 || hd < 1 || hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    if (P < 1 || P >= kTwo31 || ti < 0 || ti > (kTwo31 - 1) / P - 1) return SDM_GX_E_RANGE;
+    Shape sh{(ti + 1) * P, P, C, hd, contiguous(C, hd)};
+    int rc = validate(d_u, x, d_dv, sh, ti * P, (ti + 1) * P);
+    if (rc != SDM_GX_OK) return rc;
+    int dev = 0;
+    const DevState *dsp = nullptr;
+    rc = device_state(&dev, &dsp);
+    if (rc != SDM_GX_OK) return rc;
+    // the array holds the workspace of at most kNoAllocMaxSms CTAs: a larger device is refused, not served slower
+    if (dsp->sms > kNoAllocMaxSms) return SDM_GX_E_RANGE;
+    void *scratch = nullptr;
+    rc = noalloc_scratch(dev, &scratch);
+    if (rc != SDM_GX_OK) return rc;
+    Launch l;
+    rc = build_launch(d_u, x, d_dv, sh, ti * P, P, 0u, &l, scratch, kNoAllocScratchBytes);
+    if (rc != SDM_GX_OK) return rc;
+    return launch(l, ti, stream, pdl);
+}
+
 int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int64_t P, int64_t C, int64_t hd,
                          cudaStream_t stream, int pdl) {
     if (d_dv == nullptr || S == nullptr) return SDM_GX_E_NULL;

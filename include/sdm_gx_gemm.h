@@ -137,6 +137,22 @@ SDM_GX_API int sdm_gx_gemm_geometry(const float *d_u, const float *x, const floa
                          int64_t hd, const sdm_gx_strides *strides, unsigned flags, sdm_gx_geom *out);
 
 /*
+ * One step exactly as sdm_gx_gemm_step (same operands, checks, results and stream semantics), but the step may use the
+ * stream kernel without a plan: its workspace is a static device array inside the library (about 10 MiB per device,
+ * sized for devices of up to 160 SMs), so the call allocates nothing, ever. The pages have no counterpart to this
+ * entry point; it exists for callers that must not allocate device memory and hold no plan.
+ * Extra error: SDM_GX_E_RANGE also when the device has more than 160 SMs (the array is too small for it).
+ * The first call on a device zero-fills the array's flags and launch counters and synchronises the device.
+ * Races: every call on a device shares the one array. Calls whose kernels may overlap in time -- on different
+ * streams without an ordering between them, or from several host threads onto unordered streams -- race on the
+ * partial sums and flags and can return wrong results or report a device error. Order all calls of this entry point
+ * on one device, e.g. issue them on one stream (with pdl as for sdm_gx_gemm_step: a step touches the array only after
+ * its grid-dependency wait). Plans never use the array.
+ */
+SDM_GX_API int sdm_gx_gemm_step_noalloc(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t P, int64_t C,
+                                        int64_t hd, cudaStream_t stream, int pdl);
+
+/*
  * Plans (the page's gx_gemm_plan / gx_gemm_plan_launch): validate once, launch many steps with only ti changing.
  * plan_create runs every check of sdm_gx_gemm_step_ex for ti = ti_max (which covers every ti <= ti_max), picks the
  * kernel and tile configuration, sets the kernel attributes, and encodes the TMA descriptors of the whole tensors.
