@@ -40,8 +40,8 @@ import synth  # noqa: E402
 
 METRIC = "µs/step and GFLOP/s of d_u update; % of FP32/HBM roofline (1×GB300)"
 FP32_LANES_PER_SM = 128
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gx_tma_traffic.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "fp32_gemm_gb300", "csrc", f) for f in ("gx_tma.cu", "gx_device.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "fp32_gemm_gb300", "csrc", f) for f in ("gx_tma.cu", "gx_device.cuh", "gx_internal.h")]
 
 
 def kernel_sha() -> str:
@@ -239,7 +239,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         S = torch.from_numpy(synth.make_source(w, seed=rank)).to(dev)
     torch.cuda.synchronize()
     gx.device_error(clear=True)
-    plan = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P)
+    plan = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P, workspace=not args.no_workspace)
     geom = plan.geometry()
     # the T-step chain captured once into a CUDA graph by the library (sdm_gx_gemm_plan_graph_create)
     graph = plan.graph(0, w.T, pdl=True, S=S)
@@ -393,6 +393,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=None, help="reference arm: seconds of oracle work per step")
+    ap.add_argument("--no-workspace", action="store_true",
+                    help="plans without a workspace (tile kernels only; the stream kernel needs one)")
     ap.add_argument("--successor", action="store_true",
                     help="also time the chain with the synthetic successor after every step (hand-off cost)")
     args = ap.parse_args()
