@@ -502,3 +502,20 @@ def test_stream_workspace_rules():
                                       w.hd, ctypes.byref(s), 0, 0, base, n)
     assert rc == 0
     L.sdm_gx_gemm_plan_destroy(h)
+
+
+def test_stream_kernel_strided_rows():
+    """The stream kernel on row-padded views (leading dimension hd + 4 for d_u and d_dv, C + 4 for x: strided, still
+    TMA-eligible): the tensor maps carry the strides, the hand-off does not depend on them."""
+    k = _stream_config()
+    w = synth.Workload("stream_ld", 73, T=2, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [1, 0])
+    du, dx, dv = _dev(inp, row_pad=4)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+    assert pl.geometry()["config"] == k
+    pl.run(1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "stream kernel, padded rows")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, "stream kernel, padded rows")
