@@ -612,7 +612,10 @@ int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const float *x, co
             return SDM_GX_E_DEVICE;
         unsigned char *ctl0 = reinterpret_cast<unsigned char *>(l.tma.flags);
         const size_t nctl = 2 * static_cast<size_t>(reinterpret_cast<unsigned char *>(l.tma.ctl) - ctl0);
-        if ((e = cudaMemset(ctl0, 0, nctl)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
+        // synchronise first too: the caller's allocator may have handed out memory whose previous user still has
+        // work in flight on another stream
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess || (e = cudaMemset(ctl0, 0, nctl)) != cudaSuccess ||
+            (e = cudaDeviceSynchronize()) != cudaSuccess)
             return fail_cuda(e);
     }
     sdm_gx_plan *pl = static_cast<sdm_gx_plan *>(std::malloc(sizeof(sdm_gx_plan)));

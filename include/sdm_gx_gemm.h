@@ -171,7 +171,7 @@ SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const floa
  * this split is ours, for SM balance (e.g. 256 tiles on 152 SMs).
  *   workspace: device memory of the current device, 256-byte aligned, not overlapping d_u, x or d_dv, at least
  *   sdm_gx_gemm_plan_workspace_size() bytes; NULL (or too small) gives the plan of sdm_gx_gemm_plan_create.
- *   The call zero-fills the workspace's control words and waits for that (a device synchronisation).
+ *   The call synchronises the device, zero-fills the workspace's control words and waits for that.
  *   The workspace belongs to the plan until it is destroyed: no other plan may use it, and the steps of this plan
  *   must run one after the other (stream-ordered, as sdm_gx_gemm_plan_run, the graph and the host driver launch
  *   them; with PDL each step touches the workspace only after its grid-dependency wait). Steps of one plan running

@@ -519,3 +519,19 @@ def test_stream_kernel_strided_rows():
     assert_bitwise(du.host(), want, "stream kernel, padded rows")
     assert du.guards_intact()
     _check_untouched(dx, dv, inp, "stream kernel, padded rows")
+
+
+def test_run_host_stream_kernel():
+    """The host-buffer driver on a shape the plan runs with the stream kernel (its workspace held by the plan), as the
+    bench's end-to-end leg does on the large workload: two calls in a row match the oracle applied twice."""
+    w = synth.Workload("host_stream", 74, T=4, P=200, C=64, hd=64, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, list(range(w.T)) * 2)
+    host = {k: torch.from_numpy(v.copy()).pin_memory() for k, v in inp.items()}
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    pl = gx.Plan(dev["d_u"], dev["x"], dev["d_dv"], w.P, flags=gx.config_flag(_stream_config()))
+    d2h = pl.run_host(host["d_u"], host["x"], host["d_dv"])
+    d2h = pl.run_host(host["d_u"], host["x"], host["d_dv"])
+    d2h.synchronize()
+    torch.cuda.synchronize()
+    assert_bitwise(host["d_u"].numpy(), want, "run_host stream kernel x2")
