@@ -74,31 +74,81 @@ __device__ __forceinline__ Tile decode_tile(const TmaParams &p, int t) {
     return Tile{p.n_base + pp, ib * Cfg::TI, cb * Cfg::TC};
 }
 
+// One j of the chain: the thread's x and d_dv fragments of row jj, then its RM x RN FMAs.
+template <class Cfg>
+__device__ __forceinline__ void chain_j(const float *__restrict__ xs, const float *__restrict__ ds, int jj,
+                                        const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                        float (&acc)[Cfg::RM][Cfg::RN]) {
+    float a[Cfg::RM], b[Cfg::RN];
+#pragma unroll
+    for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
+#pragma unroll
+    for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+    if constexpr (Cfg::RM % 2 == 0) {
+        // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
+#pragma unroll
+        for (int c = 0; c < Cfg::RN; ++c) {
+#pragma unroll
+            for (int r = 0; r < Cfg::RM; r += 2) dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+            for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+        }
+    }
+}
+
 // The chain for nj consecutive j of one stage (j order preserved: jj ascending).
+//
+// The same loop is spelt three ways because the compiler schedules them differently and each kernel family keeps
+// the spelling it measured fastest with (differences of 1-2% on the large step, 17% on tiny steps):
+//   * a full stage: the inline body under one unroll (tile and slab kernels), or the per-j helper (stream kernel);
+//   * a partial stage (the ragged end of C, or the end of a piece in the stream kernel): blocks of four unrolled j,
+//     then one at a time (stream kernel and the small tiles, where C below the stage size makes every stage
+//     partial), or the full-stage loop with a run-time count (the large tiles and the slab kernel, whose full stages
+//     lose when the blocked form is compiled beside them).
 template <class Cfg, bool FULL>
 __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const float *__restrict__ ds,
                                             const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
                                             float (&acc)[Cfg::RM][Cfg::RN], int nj) {
-    const int cnt = FULL ? Cfg::KB : nj;
+    constexpr bool kHelper = Cfg::SLAB == 2;
+    constexpr bool kBlocked = Cfg::SLAB == 2 || (Cfg::SLAB == 0 && Cfg::RM * Cfg::RN < 32);
+    if constexpr (FULL && kHelper) {
 #pragma unroll(Cfg::UNROLL)
-    for (int jj = 0; jj < cnt; ++jj) {
-        float a[Cfg::RM], b[Cfg::RN];
+        for (int jj = 0; jj < Cfg::KB; ++jj) chain_j<Cfg>(xs, ds, jj, ro, co, acc);
+    } else if constexpr (!FULL && kBlocked) {
+        int jj = 0;
+        for (; jj + 4 <= nj; jj += 4) {
 #pragma unroll
-        for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
+            for (int u = 0; u < 4; ++u) chain_j<Cfg>(xs, ds, jj + u, ro, co, acc);
+        }
+#pragma unroll 1
+        for (; jj < nj; ++jj) chain_j<Cfg>(xs, ds, jj, ro, co, acc);
+    } else {
+        const int cnt = FULL ? Cfg::KB : nj;
+#pragma unroll(Cfg::UNROLL)
+        for (int jj = 0; jj < cnt; ++jj) {
+            float a[Cfg::RM], b[Cfg::RN];
 #pragma unroll
-        for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
-        if constexpr (Cfg::RM % 2 == 0) {
-            // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
+            for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
 #pragma unroll
-            for (int c = 0; c < Cfg::RN; ++c) {
+            for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+            if constexpr (Cfg::RM % 2 == 0) {
+                // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
 #pragma unroll
-                for (int r = 0; r < Cfg::RM; r += 2) dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
-            }
-        } else {
+                for (int c = 0; c < Cfg::RN; ++c) {
 #pragma unroll
-            for (int r = 0; r < Cfg::RM; ++r) {
+                    for (int r = 0; r < Cfg::RM; r += 2)
+                        dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
+                }
+            } else {
 #pragma unroll
-                for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+                for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+                    for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+                }
             }
         }
     }
@@ -597,7 +647,8 @@ struct KCfg : T {
     // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
     static constexpr int NBAR = 2 * T::ST + 6;
     static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
-    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8 + 4, 128) + 128;
+    static constexpr int OFF_PIECES = align_up(OFF_EPOCH + 4, 16);   // the CTA's Pieces (computed once)
+    static constexpr int SMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128) + 128;
     static_assert((T::TI * T::TC * 4) % 16 == 0, "the partial-sum tile is copied in 16-byte units");
 };
 
@@ -666,10 +717,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_stream_kernel(const __grid
         dev::mbar_init(head_stored, 1);
         dev::mbar_init(epoch_known, 1);
         dev::fence_mbar_init();
+        *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G);
     }
     __syncthreads();
-
-    const Pieces R = cta_pieces(p.ntiles, p.C, b, G);
+    // read from shared memory where needed, so that no thread keeps the descriptor in registers
+    const Pieces &R = *reinterpret_cast<const Pieces *>(base_g + Cfg::OFF_PIECES);
 
     if (warp == Cfg::NCW + 1) {
         // ------------------------------------------------ publisher -----------------------------------------------
