@@ -176,6 +176,8 @@ SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const floa
  *   must run one after the other (stream-ordered, as sdm_gx_gemm_plan_run, the graph and the host driver launch
  *   them; with PDL each step touches the workspace only after its grid-dependency wait). Steps of one plan running
  *   concurrently on unordered streams would race on it.
+ * The stream kernel runs one CTA per SM and expects all of them resident together (a whole GPU); under a context
+ * limited to fewer SMs, create the plan without a workspace.
  * Errors as sdm_gx_gemm_plan_create, plus SDM_GX_E_ALIGN / SDM_GX_E_OVERLAP / SDM_GX_E_DEVICE for the workspace.
  */
 SDM_GX_API int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N,
