@@ -237,6 +237,22 @@ print(json.dumps(done))
 """
 
 
+def host_cpu() -> str:
+    """The host CPU as lscpu names it, with the architecture (the oracle's fmaf is the hardware fused multiply-add
+    there: inline FMADD on aarch64, glibc's FMA path on x86-64 CPUs that have FMA)."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return f"{model or 'unknown model'} ({platform.machine()}, {os.cpu_count()} cores)"
+
+
 def cpu_oracle_parallel(w: synth.Workload, per: float, nwin: int, workers: int) -> list:
     """The oracle (as it stands) on all `workers` host cores at once, one process per core over independent chunks
     (the chains of different chunks share nothing, so the bits are those of one thread). Returns, per window, the
@@ -461,6 +477,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
                 "config": {"workload": w.name, "T": w.T, "P": w.P, "C": w.C, "hd": w.hd},
                 "cpu_baseline": {"value": round(v, 4), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
+                                 "cpu": host_cpu(),
                                  "sample": f"whole chunks (C={w.C}, hd={w.hd}) of the {w.name} workload, one oracle "
                                            f"process per core over different chunks, {per:.1f} s per step; median of "
                                            f"{args.steps} steps"},
@@ -481,7 +498,8 @@ def main():
             out["cpu_baseline"] = {"value": round(par, 4), "unit": "GFLOP/s", "cores": cores, "kind": "oracle",
                                    "sample": f"whole chunks (C={w.C}, hd={w.hd}) of the {w.name} workload for "
                                              f"{sec:.1f} s, one oracle process per core over different chunks",
-                                   "single_thread": {"value": round(single["value"], 4), "sample": single["sample"]}}
+                                   "single_thread": {"value": round(single["value"], 4), "sample": single["sample"]},
+                                   "cpu": host_cpu()}
         if rank == 0:
             print(json.dumps(out), flush=True)
     finally:
