@@ -261,6 +261,7 @@ def test_large_full_size_bench_configuration_sampled():
     d = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
     pl = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P)
     assert pl.geometry() == gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P).geometry()
+    assert gx.config_info(1, pl.geometry()["config"])["kind"] == "stream"   # the kernel bench.py times
     g = pl.graph(0, w.T, pdl=True)
     g.launch()
     torch.cuda.synchronize()
