@@ -536,3 +536,24 @@ def test_run_host_stream_kernel():
     d2h.synchronize()
     torch.cuda.synchronize()
     assert_bitwise(host["d_u"].numpy(), want, "run_host stream kernel x2")
+
+
+@pytest.mark.parametrize("vset", synth.VALUE_SETS)
+def test_stream_kernel_value_sets(vset):
+    """The stream kernel on every value set (zeros and signed zeros, 1e30-scale overflow, the wide range, subnormals,
+    +-Inf, NaN): the FP32 accumulators handed between CTAs through shared memory, bulk copies and the workspace keep
+    their bits (NaN as a class), and no output is -0. 160 chunks of 48 x 100: every hand-off is tight."""
+    k = _stream_config()
+    w = synth.Workload("stream_vs", 75, T=2, P=160, C=48, hd=100, x_scale="unit")
+    inp = synth.make_inputs(w, value_set=vset)
+    want, _ = _oracle_steps(inp, w.P, [0, 1])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+    assert pl.geometry()["config"] == k
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"stream kernel, {vset}")
+    assert du.guards_intact()
+    got = du.host()
+    zero = (got == 0) & ~np.isnan(got)
+    assert not np.any(np.signbit(got[zero])), "a -0 output"
