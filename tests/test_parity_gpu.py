@@ -426,12 +426,13 @@ def _stream_config():
 
 
 @pytest.mark.parametrize("P,C,hd,T", [(160, 100, 76, 2), (153, 64, 64, 2), (100, 128, 200, 2), (304, 128, 128, 2),
-                                      (200, 32, 500, 2), (256, 128, 128, 2)])
+                                      (200, 32, 500, 2), (256, 128, 128, 2), (1000, 32, 64, 2), (160, 256, 128, 2)])
 def test_stream_kernel_shapes(P, C, hd, T):
     """The stream kernel (a step's (tile, j) work split evenly over one CTA per SM; chains continued across CTAs from
     the accumulators left in the plan's workspace): ragged rows and columns, one tile more than SMs (hand-offs with
-    almost no slack), several column blocks, exactly two tiles per CTA (no split), the large step. The chain is
-    captured into a graph and replayed twice, so the workspace's launch epoch advances over 2T launches."""
+    almost no slack), several column blocks, exactly two tiles per CTA (no split), the large step, many whole tiles
+    per CTA (1000 tiles), and C = 256 (two row blocks per chunk). The chain is captured into a graph and replayed
+    twice, so the workspace's launch epoch advances over 2T launches."""
     k = _stream_config()
     w = synth.Workload("stream", 68, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
