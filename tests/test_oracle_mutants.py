@@ -4,7 +4,6 @@
 import ctypes
 import os
 import subprocess
-import tempfile
 
 import numpy as np
 import pytest
@@ -38,7 +37,9 @@ def _build_mutant(name):
     src = SRC.replace(old, new)
     # keep the environment self-check from rejecting the unfused mutant before the pins can
     src = src.replace("if (!oracle_fp_env_ok()) return -1;", "")
-    d = tempfile.mkdtemp(prefix="oracle_mutant_")
+    # scratch inside the repository (the oracle's own git-ignored build folder), one folder per mutant
+    d = os.path.join(os.path.dirname(oracle.__file__), "_build", "mutants", name)
+    os.makedirs(d, exist_ok=True)
     c = os.path.join(d, "m.c")
     so = os.path.join(d, "m.so")
     open(c, "w").write(src)
