@@ -459,12 +459,15 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     return SDM_GX_OK;
 }
 
-int launch(const Launch &l, int64_t ti, cudaStream_t st, int pdl) {
+// dv_rewritten: the kernel right before this step writes the step's d_dv (the producer chain), so an L2 prefetch of
+// d_dv before the dependency wait would fetch lines that are about to be replaced; it is skipped.
+int launch(const Launch &l, int64_t ti, cudaStream_t st, int pdl, bool dv_rewritten = false) {
     const int64_t nb = ti * l.P - l.n_first;
     cudaError_t e;
     if (l.path == 1) {
         TmaParams p = l.tma;
         p.n_base = static_cast<int32_t>(nb);
+        if (dv_rewritten) p.prefetch = 0;
         e = tma_launch(l.config, p, l.grid, st, pdl);
     } else {
         GenericParams p = l.gen;
@@ -689,7 +692,7 @@ int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64
             g_count_producer.fetch_add(1, std::memory_order_relaxed);
             if (pdl) g_count_pdl.fetch_add(1, std::memory_order_relaxed);
         }
-        rc = launch(plan->launch, ti, stream, pdl);
+        rc = launch(plan->launch, ti, stream, pdl, true);
         if (rc != SDM_GX_OK) return rc;
     }
     return SDM_GX_OK;

@@ -203,7 +203,8 @@ SDM_GX_API int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, i
 
 /* The same driver with the synthetic producer in the chain: before each step ti it launches the producer, which
  * writes d_dv chunks of step ti from S (S has d_dv's shape and strides; see sdm_gx_producer_step). Producer and step
- * launches alternate on `stream`; with pdl != 0 each is a programmatic dependent launch of the one before. */
+ * launches alternate on `stream`; with pdl != 0 each is a programmatic dependent launch of the one before. The steps
+ * of this driver skip the L2 prefetch of d_dv before their dependency wait (the producer is about to rewrite it). */
 SDM_GX_API int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const float *S, int64_t ti_begin, int64_t ti_end,
                                   cudaStream_t stream, int pdl);
 
