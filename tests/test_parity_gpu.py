@@ -74,7 +74,14 @@ def _ragged_workload():
     return synth.Workload("ragged", 60, T=2, P=3, C=100, hd=76, x_scale="inv_sqrt_c")
 
 
-@pytest.mark.parametrize("config", list(range(32)))
+MAX_TMA_CONFIGS = 16   # the parametrisation below covers every configuration while the menu stays within this
+
+
+def test_config_menu_covered():
+    assert gx.num_configs(1) <= MAX_TMA_CONFIGS, "extend MAX_TMA_CONFIGS so that every configuration is tested"
+
+
+@pytest.mark.parametrize("config", list(range(MAX_TMA_CONFIGS)))
 def test_every_tma_config_ragged(config):
     if config >= gx.num_configs(1):
         pytest.skip("no such configuration")
