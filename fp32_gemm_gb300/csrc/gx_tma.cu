@@ -1,4 +1,6 @@
-// The TMA-fed, warp-specialised FP32 kernel of the gx_gemm step update (sm_103a).
+// The TMA-fed, warp-specialised FP32 kernels of the gx_gemm step update (sm_103a): the tile kernel (gx_tma_kernel),
+// the balanced slab kernel (gx_slab_kernel) and the stream kernel (gx_stream_kernel), which share the pipeline, the
+// chain and the epilogue described here and differ in how a step's work is cut over the CTAs.
 //
 // What it computes (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring formula and gx_gemm_kernel): for every
 // chunk n of the step, row i < C and column c < hd, one thread runs acc = +0; acc = fmaf(x[n,j,i], d_dv[n,j,c], acc)
@@ -12,7 +14,8 @@
 //     xs[KB][TI] (x rows j, columns i) and ds[KB][TC] (d_dv rows j, columns c). mbarrier full/empty pairs with
 //     transaction counts hand stages between producer and consumers. The d_u tile [TI][TC] is staged the same way.
 //   * Consumer warps hold an RM x RN register tile per thread (4 x 8 lanes per warp, rows and columns in vectors of
-//     up to 4) and run the j-chain in order with fmaf: per j, RM/4 + RN/4 vector shared loads feed RM*RN FMAs.
+//     up to 4) and run the j-chain in order with fmaf (rows in pairs as packed fma.rn.f32x2, bit-identical): per j,
+//     RM/4 + RN/4 vector shared loads feed RM*RN FMAs.
 //   * Programmatic dependent launch: before griddepcontrol.wait the producer issues the first tile's d_u box and the
 //     x boxes of the first ST stages, and prefetches that tile's d_dv boxes into L2 (no visible effect: L2 is the
 //     point of coherence). d_dv is loaded into shared memory only after the wait; d_u is written only after it.
