@@ -22,7 +22,7 @@ HEADERS = ("gx_internal.h", "gx_device.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-Xcompiler", "-fvisibility=hidden",
-              "-diag-suppress", "1160"]
+              "-diag-suppress", "1160", "-diag-suppress", "177"]
 
 
 def _nvcc() -> str:

@@ -214,6 +214,12 @@ struct Launch {
 // j-chain's dependent-FMA latency) for every tile it runs in sequence.
 double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
     const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+    const double tile_fma = static_cast<double>(ci.TI) * ci.TC * C;
+    // FMA rate of an SM running n CTAs of this configuration: the measured efficiency, scaled down while fewer than
+    // eight consumer warps share the SM
+    auto rate = [&](int64_t n) {
+        return 128.0 * (ci.eff / 100.0) * std::min(1.0, static_cast<double>(n * ci.consumer_warps) / 8.0);
+    };
     if (ci.kind == 1) {
         // balanced slabs: every SM gets at most ceil(slabs / SMs), in rounds of four on 16 warps; a partial round of
         // k slabs costs about 1 + 0.9 k slabs (measured: its fixed part does not shrink with k)
@@ -221,46 +227,53 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
         const int64_t full = per_sm / 4, k = per_sm % 4;
         const double eq = 4.0 * static_cast<double>(full) + (k ? 1.0 + 0.9 * static_cast<double>(k) : 0.0);
         const int64_t rounds = (per_sm + 3) / 4;
-        const double rate = 128.0 * (ci.eff / 100.0);
-        return eq * ci.TI * ci.TC * C / rate + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
+        return eq * tile_fma / rate(2) + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
     }
     if (ci.kind == 2) {
-        // (tile, j) units split evenly over one CTA per SM; a CTA runs up to two partial pieces besides its whole
-        // tiles, and the hand-off of partial sums costs about one k-block's latency
-        const double units = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
-        const double rate = 128.0 * (ci.eff / 100.0);
-        const double pieces = std::ceil(units / static_cast<double>(C)) + 1.0;
-        return units * ci.TI * ci.TC / rate + pieces * (1500.0 + 8.0 * C) + 2000.0;
+        // (tile, j) units split evenly over every resident CTA (occ per SM, all busy to the end); each CTA runs up to
+        // two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one k-block
+        const double units_sm = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
+        const double units_cta = units_sm / std::max(1, occ);
+        const double pieces = std::ceil(units_cta / static_cast<double>(C)) + 1.0;
+        return units_sm * ci.TI * ci.TC / rate(occ) + pieces * (1500.0 + 8.0 * C) + 2000.0;
     }
+    // whole tiles: an SM runs rounds of up to `occ` concurrent CTAs; a last round with fewer CTAs runs at its own
+    // (lower) rate, and each round pays a per-tile cost (pipeline fill, epilogue, the chain's dependent latency)
     const int64_t per_sm = (tiles + sms - 1) / sms;
     const int64_t a = std::min<int64_t>(occ, per_sm);
-    const int64_t seq = (per_sm + a - 1) / a;
-    const double util = std::min(1.0, static_cast<double>(a * ci.consumer_warps) / 8.0);
-    const double rate = 128.0 * (ci.eff / 100.0) * util;
-    const double work = static_cast<double>(per_sm) * ci.TI * ci.TC * C;
-    return work / rate + static_cast<double>(seq) * (1500.0 + 8.0 * C);
+    const int64_t full = per_sm / a, rem = per_sm % a;
+    double t = static_cast<double>(full) * static_cast<double>(a) * tile_fma / rate(a);
+    if (rem) t += static_cast<double>(rem) * tile_fma / rate(rem);
+    return t + static_cast<double>(full + (rem ? 1 : 0)) * (1500.0 + 8.0 * C);
 }
 
 // The slab kernel needs whole 32-row slabs (C % 32 == 0) and at most two (chunk, column block) per round of four
-// consecutive slabs (C / 32 >= 3). The stream kernel needs the plan's workspace (ws_bytes at least its size) and at
-// least as many tiles as SMs, so that every CTA's range of (tile, j) units is at least one tile long.
-bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int sms, size_t ws_bytes) {
+// consecutive slabs (C / 32 >= 3). The stream kernel runs `stream_ctas` CTAs (every resident slot: SMs x CTAs per
+// SM), needs the plan's workspace sized for them (ws_bytes), and at least as many tiles as CTAs, so that every CTA's
+// range of (tile, j) units is at least one tile long.
+bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int stream_ctas, size_t ws_bytes) {
     if (ci.kind == 1) return C % ci.TI == 0 && C / ci.TI >= 3;
     if (ci.kind == 2) {
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
-        return tiles >= sms && ws_bytes >= stream_workspace_bytes(sms, ci.TI, ci.TC);
+        return stream_ctas >= 1 && tiles >= stream_ctas &&
+               ws_bytes >= stream_workspace_bytes(stream_ctas, ci.TI, ci.TC);
     }
     return true;
 }
 
-int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes) {
+// the stream kernel's grid for configuration k on this device: one CTA per resident slot
+int stream_ctas_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_occ[k]); }
+
+int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes,
+                      int max_stream_ctas) {
     if (forced >= 0) return forced;
     auto tiles_of = [&](const ConfigInfo &ci) {
         return P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
     };
     auto usable = [&](int k) {
         const ConfigInfo &ci = tma_config(k);
-        return d.tma_occ[k] >= 1 && config_eligible(ci, P, C, hd, d.sms, ws_bytes) && !(ci.kind == 1 && !d.slab_ok) &&
+        return d.tma_occ[k] >= 1 && config_eligible(ci, P, C, hd, stream_ctas_of(d, k), ws_bytes) &&
+               !(ci.kind == 2 && stream_ctas_of(d, k) > max_stream_ctas) && !(ci.kind == 1 && !d.slab_ok) &&
                tiles_of(ci) < kTwo31;
     };
     // Small steps (no tile of 32+ outputs per thread fills the SMs): the step is bound by latency, and the measured
@@ -326,8 +339,12 @@ CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t ro
 
 // Build the launch description for chunks n_first .. n_first + n_count - 1 (pointers and tensor maps originate at
 // n_first). Runs after validate(); makes CUDA calls (device state, descriptor encoding).
+// ws / ws_bytes: the plan's workspace (or none). fixed_part_bytes != 0 puts the workspace's flags and launch counters
+// at that fixed offset whatever the configuration (the shared static array of sdm_gx_gemm_step_noalloc), and
+// max_stream_ctas bounds the stream kernel's grid there.
 int build_launch(float *du, const float *x, const float *dv, const Shape &sh, int64_t n_first, int64_t n_count,
-                 unsigned flags, Launch *L, void *ws = nullptr, size_t ws_bytes = 0) {
+                 unsigned flags, Launch *L, void *ws = nullptr, size_t ws_bytes = 0, size_t fixed_part_bytes = 0,
+                 int max_stream_ctas = 1 << 30) {
     const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
                            SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL;
     if (flags & ~known) return SDM_GX_E_FLAGS;
@@ -363,14 +380,15 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     int occ = 0;
     if (use_tma) {
         if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
-        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0);
+        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, max_stream_ctas);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
-        if (!config_eligible(*ci, sh.P, sh.C, sh.hd, d.sms, ws != nullptr ? ws_bytes : 0) ||
+        if (!config_eligible(*ci, sh.P, sh.C, sh.hd, stream_ctas_of(d, k), ws != nullptr ? ws_bytes : 0) ||
+            (ci->kind == 2 && stream_ctas_of(d, k) > max_stream_ctas) ||
             (ci->kind == 1 && !d.slab_ok))
             return SDM_GX_E_FLAGS;
         if (ci->smem > d.optin || d.tma_occ[k] < 1) return SDM_GX_E_SMEM;
-        occ = ci->kind == 2 ? 1 : d.tma_occ[k];
+        occ = d.tma_occ[k];
         l.path = 1;
         l.config = k;
         TmaParams &t = l.tma;
@@ -404,8 +422,11 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         t.stall_test = (flags & SDM_GX_FLAG_TEST_STALL) ? 1 : 0;
         if (ci->kind == 2) {   // workspace: partial sums, flags, control words (sizes as stream_workspace_bytes)
             unsigned char *w = static_cast<unsigned char *>(ws);
-            const size_t part = (static_cast<size_t>(d.sms) * ci->TI * ci->TC * 4 + 255) / 256 * 256;
-            const size_t fl = (static_cast<size_t>(d.sms) * 4 + 255) / 256 * 256;
+            const int G = stream_ctas_of(d, k);
+            const size_t need = (static_cast<size_t>(G) * ci->TI * ci->TC * 4 + 255) / 256 * 256;
+            const size_t part = fixed_part_bytes ? fixed_part_bytes : need;
+            const size_t fl = (static_cast<size_t>(fixed_part_bytes ? max_stream_ctas : G) * 4 + 255) / 256 * 256;
+            if (part < need || part + 2 * fl > ws_bytes) return SDM_GX_E_FLAGS;
             t.part = reinterpret_cast<float *>(w);
             t.flags = reinterpret_cast<uint32_t *>(w + part);
             t.ctl = reinterpret_cast<uint32_t *>(w + part + fl);
@@ -439,8 +460,9 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     if (forced_occ > 0) occ = std::min(occ, forced_occ);
     const int64_t tiles = l.path ? l.tma.ntiles : l.gen.ntiles;
     const int64_t slots = static_cast<int64_t>(d.sms) * occ;
-    // the stream kernel runs one CTA per SM (its workspace is sized for that grid)
-    l.grid = (ci->kind == 2 && l.path == 1) ? d.sms : static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
+    // the stream kernel runs one CTA per resident slot (its workspace is sized for that grid)
+    l.grid = (ci->kind == 2 && l.path == 1) ? static_cast<int>(slots)
+                                             : static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
     sdm_gx_geom &gm = l.geom;
     gm.path = l.path;
     gm.config = l.config;
@@ -575,8 +597,9 @@ int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const floa
     for (int k = 0; k < tma_num_configs(); ++k) {
         const ConfigInfo &ci = tma_config(k);
         if (ci.kind != 2 || dsp->tma_occ[k] < 1) continue;
-        const size_t b = stream_workspace_bytes(dsp->sms, ci.TI, ci.TC);
-        if (config_eligible(ci, P, C, hd, dsp->sms, b)) need = std::max(need, b);
+        const int G = stream_ctas_of(*dsp, k);
+        const size_t b = stream_workspace_bytes(G, ci.TI, ci.TC);
+        if (config_eligible(ci, P, C, hd, G, b)) need = std::max(need, b);
     }
     *bytes = need;
     return SDM_GX_OK;
@@ -910,7 +933,10 @@ void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan) {
 // ---- the entry point that allocates nothing --------------------------------------------------------------------------
 // Its scratch is one static device array per device (each device's module instance has its own copy), used as the
 // stream kernel's workspace: partial sums for up to kNoAllocMaxSms CTAs of 128 x 128 tiles, then flags, then launch
-// counters, laid out as stream_workspace_bytes describes. No call allocates; every call shares the array.
+// counters. The flags and counters sit at that fixed offset whatever the tile shape, and the stream kernel's grid is
+// bounded by kNoAllocMaxSms (configurations with one CTA per SM), so that every launch on the array counts the same
+// CTAs and the per-CTA launch counters stay equal across calls of different shapes. No call allocates; every call
+// shares the array.
 namespace {
 constexpr int kNoAllocMaxSms = 160;
 constexpr size_t kNoAllocWords = (static_cast<size_t>(kNoAllocMaxSms) * 4 + 255) / 256 * 256;
@@ -963,7 +989,8 @@ int sdm_gx_gemm_step_noalloc(float *d_u, const float *x, const float *d_dv, int6
     rc = noalloc_scratch(dev, &scratch);
     if (rc != SDM_GX_OK) return rc;
     Launch l;
-    rc = build_launch(d_u, x, d_dv, sh, ti * P, P, 0u, &l, scratch, kNoAllocScratchBytes);
+    rc = build_launch(d_u, x, d_dv, sh, ti * P, P, 0u, &l, scratch, kNoAllocScratchBytes,
+                      kNoAllocScratchBytes - 2 * kNoAllocWords, kNoAllocMaxSms);
     if (rc != SDM_GX_OK) return rc;
     return launch(l, ti, stream, pdl);
 }

@@ -690,7 +690,7 @@ __device__ __forceinline__ void load_frag(const float *src, int tid, float (&acc
 }
 
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, 1) gx_stream_kernel(const __grid_constant__ TmaParams p) {
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_s = dev::smem_addr(smem_raw);
     const uint32_t base_s = (raw_s + 127u) & ~127u;
@@ -986,6 +986,7 @@ using C9 = TCfg<4, 4, 1, 1, 32, 2, 8, 25>;   //  16 x  32,  1 warp
 using C10 = TCfg<2, 4, 1, 1, 32, 2, 8, 20>;  //   8 x  32,  1 warp
 using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 warps (rounds of four slabs)
 using C12 = KCfg<C0, 72>;                     // C0's tile with the (tile, j) work split evenly over the CTAs
+using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128 x 64 tiles, 8 warps, 2 CTAs per SM
 
 struct Entry {
     ConfigInfo info;
@@ -996,7 +997,7 @@ struct Entry {
 #define SDMGX_ENTRY(C) Entry{info_of<C>(), kernel_of<C>(), &launch_cfg<C>}
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
-                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12)};
+                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13)};
 #undef SDMGX_ENTRY
 
 }  // namespace

@@ -164,7 +164,8 @@ SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const floa
 
 /*
  * A plan with a workspace. With a large enough workspace the plan may pick the stream kernel: the step's work, in
- * units of (tile, j), split evenly over one CTA per SM instead of in whole tiles. A CTA then runs the first j of one
+ * units of (tile, j), split evenly over every resident CTA (one or two per SM, by tile shape) instead of in whole
+ * tiles. A CTA then runs the first j of one
  * tile and another CTA continues those outputs' chains from the FP32 accumulators that the first one left in the
  * workspace. Each output still gets the one fixed chain acc = fmaf(x, d_dv, acc) for j = 0..C-1 from +0 and the one
  * final add, so the results are bit for bit those of every other kernel. The pages split work only in whole chunks;
@@ -176,8 +177,8 @@ SDM_GX_API int sdm_gx_gemm_plan_create(sdm_gx_plan **out, float *d_u, const floa
  *   must run one after the other (stream-ordered, as sdm_gx_gemm_plan_run, the graph and the host driver launch
  *   them; with PDL each step touches the workspace only after its grid-dependency wait). Steps of one plan running
  *   concurrently on unordered streams would race on it.
- * The stream kernel runs one CTA per SM and expects all of them resident together (a whole GPU); under a context
- * limited to fewer SMs, create the plan without a workspace.
+ * The stream kernel runs one CTA per resident slot and expects all of them resident together (a whole GPU); under a
+ * context limited to fewer SMs, create the plan without a workspace.
  * Errors as sdm_gx_gemm_plan_create, plus SDM_GX_E_ALIGN / SDM_GX_E_OVERLAP / SDM_GX_E_DEVICE for the workspace.
  */
 SDM_GX_API int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const float *x, const float *d_dv, int64_t N,
@@ -185,7 +186,8 @@ SDM_GX_API int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const f
                                           int64_t ti_max, unsigned flags, void *workspace, size_t workspace_bytes);
 
 /* Bytes of workspace that lets a plan of this shape and layout use the stream kernel on the current device (0: no
- * kernel of this shape uses one). About (number of SMs) x TI x TC x 4 bytes: 9.5 MiB for 128 x 128 tiles on 152 SMs. */
+ * kernel of this shape uses one). About (resident CTAs) x TI x TC x 4 bytes: 9.5 MiB for 128 x 128 tiles on 152 SMs
+ * (one CTA per SM), the same for 128 x 64 tiles (two per SM). */
 SDM_GX_API int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const float *d_dv, int64_t N,
                                                int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides,
                                                unsigned flags, size_t *bytes);

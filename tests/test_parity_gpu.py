@@ -565,3 +565,30 @@ def test_stream_kernel_value_sets(vset):
     got = du.host()
     zero = (got == 0) & ~np.isnan(got)
     assert not np.any(np.signbit(got[zero])), "a -0 output"
+
+
+def _stream_configs():
+    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "stream"]
+
+
+@pytest.mark.parametrize("P,C,hd", [(400, 128, 64), (320, 96, 60), (600, 64, 128)])
+def test_stream_kernel_all_tile_shapes(P, C, hd):
+    """Every stream configuration (128 x 128 tiles with one CTA per SM; 128 x 64 tiles with two per SM, 304 CTAs and
+    a workspace sized for them) on shapes it splits: column blocks of 64, ragged rows and columns, many tiles per CTA.
+    A graph of the two steps, replayed twice."""
+    w = synth.Workload("stream_ts", 76, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, [1, 0] * 2)
+    for k in _stream_configs():
+        du, dx, dv = _dev(inp)
+        pl = gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(k))
+        g = pl.geometry()
+        info = gx.config_info(1, k)
+        assert g["config"] == k and g["ctas"] == g["sms"] * g["ctas_per_sm"], (g, info)
+        gr = pl.graph(1, -1, pdl=True)
+        gr.launch()
+        gr.launch()
+        torch.cuda.synchronize()
+        assert_bitwise(du.host(), want, f"stream config {k} ({info['TI']} x {info['TC']}) P={P} C={C} hd={hd}")
+        assert du.guards_intact()
+        gr.close()
