@@ -123,11 +123,27 @@ def test_unknown_flags_rejected_before_cuda():
     assert rc < 0
 
 
-def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+def test_missing_library_fails_loudly(monkeypatch):
     import fp32_gemm_gb300._binding as b
-    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
+    missing = os.path.join(ROOT, "fp32_gemm_gb300", "lib", "no_such_library.so")
+    assert not os.path.exists(missing)
+    monkeypatch.setattr(b, "LIB_PATH", missing)
     with pytest.raises(ImportError):
         b._load()
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_as_c_and_cpp(lang, std):
+    """include/sdm_gx_gemm.h is a C ABI: it must compile as strict C99 and as C++ (syntax only; nothing is written)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("no host compiler or CUDA headers")
+    r = subprocess.run([cc, "-x", lang, std, "-Wall", "-Wextra", "-pedantic", "-fsyntax-only", "-I", cuda_inc, HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_binding_has_no_cpu_fallback():
