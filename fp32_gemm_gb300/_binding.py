@@ -70,6 +70,10 @@ SIGNATURES = {
                                                            ctypes.c_void_p, ctypes.c_size_t]),
     "sdm_gx_gemm_plan_workspace_size": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
                                         [ctypes.POINTER(Strides), ctypes.c_uint, ctypes.POINTER(ctypes.c_size_t)]),
+    "sdm_gx_gemm_autotune": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 4 +
+                             [ctypes.POINTER(Strides), ctypes.c_uint, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                              ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_int32),
+                              ctypes.POINTER(ctypes.c_float)]),
     "sdm_gx_gemm_plan_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_plan_run": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_int]),
@@ -205,6 +209,24 @@ def workspace_size(d_u, x, d_dv, P: int, flags: int = 0) -> int:
                                                 ctypes.byref(s), int(flags), ctypes.byref(n)),
            "sdm_gx_gemm_plan_workspace_size")
     return int(n.value)
+
+
+def autotune(d_u_scratch, x, d_dv, P: int, steps: int = 20, flags: int = 0, workspace: bool = True,
+             stream=None) -> dict:
+    """sdm_gx_gemm_autotune: time every configuration that this shape and layout admit, on these buffers, and return
+    {"flags", "config", "us"} of the fastest; Plan(d_u, x, d_dv, P, flags=result["flags"]) then uses it. d_u_scratch
+    is updated by the timed steps: pass a copy of d_u (same shape and strides), never d_u itself. workspace=True lets
+    the stream configurations take part (a temporary allocation of the size a Plan's workspace has; the Plan must then
+    have its workspace too, the default)."""
+    uv, xv, vv, N, C, hd, s = _operands(d_u_scratch, x, d_dv)
+    nws = workspace_size(d_u_scratch, x, d_dv, P, flags) if workspace else 0
+    ws = torch.empty(nws, dtype=torch.uint8, device=uv.device) if nws > 0 else None
+    fo, co, us = ctypes.c_uint(0), ctypes.c_int32(-1), ctypes.c_float(0.0)
+    _check(_lib.sdm_gx_gemm_autotune(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd, ctypes.byref(s),
+                                     int(flags), ws.data_ptr() if ws is not None else None, nws, int(steps),
+                                     _stream(stream), ctypes.byref(fo), ctypes.byref(co), ctypes.byref(us)),
+           "sdm_gx_gemm_autotune")
+    return {"flags": int(fo.value), "config": int(co.value), "us": float(us.value)}
 
 
 class Plan:

@@ -675,6 +675,70 @@ int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stre
     return launch(plan->launch, ti, stream, pdl);
 }
 
+int sdm_gx_gemm_autotune(float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C, int64_t hd,
+                         const sdm_gx_strides *strides, unsigned flags, void *workspace, size_t workspace_bytes,
+                         int steps, cudaStream_t stream, unsigned *flags_out, int32_t *config_out, float *us_out) {
+    if (flags_out == nullptr) return SDM_GX_E_NULL;
+    if (steps < 1 || steps > 4096) return SDM_GX_E_RANGE;
+    if (flags & (SDM_GX_FLAG_CONFIG_MASK | SDM_GX_FLAG_TEST_STALL)) return SDM_GX_E_FLAGS;
+    if (P < 1 || N < P) return SDM_GX_E_RANGE;
+    const int64_t T = N / P;
+    // the automatic plan validates every argument and names the path this shape and layout take
+    sdm_gx_plan *pl = nullptr;
+    int rc = sdm_gx_gemm_plan_create_ws(&pl, d_u, x, d_dv, N, P, C, hd, strides, T - 1, flags, workspace,
+                                        workspace_bytes);
+    if (rc != SDM_GX_OK) return rc;
+    const int path = pl->launch.path;
+    sdm_gx_gemm_plan_destroy(pl);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e == cudaSuccess) e = cudaEventCreate(&e1);
+    if (e != cudaSuccess) {
+        if (e0 != nullptr) cudaEventDestroy(e0);
+        return fail_cuda(e);
+    }
+    int best = -1;
+    float best_us = 0.0f;
+    const int nk = sdm_gx_gemm_num_configs(path);
+    for (int k = 0; k < nk && rc == SDM_GX_OK; ++k) {
+        sdm_gx_plan *pk = nullptr;
+        int r = sdm_gx_gemm_plan_create_ws(&pk, d_u, x, d_dv, N, P, C, hd, strides, T - 1,
+                                           flags | static_cast<unsigned>(k + 1), workspace, workspace_bytes);
+        if (r == SDM_GX_E_FLAGS || r == SDM_GX_E_SMEM) continue;   // not admitted here
+        if (r != SDM_GX_OK) {
+            rc = r;
+            break;
+        }
+        float ms = 0.0f;
+        for (int s = 0; s < 2 && r == SDM_GX_OK; ++s) r = sdm_gx_gemm_plan_step(pk, s % T, stream, 1);
+        if (r == SDM_GX_OK && (e = cudaEventRecord(e0, stream)) != cudaSuccess) r = fail_cuda(e);
+        for (int s = 0; s < steps && r == SDM_GX_OK; ++s) r = sdm_gx_gemm_plan_step(pk, s % T, stream, 1);
+        if (r == SDM_GX_OK && (e = cudaEventRecord(e1, stream)) != cudaSuccess) r = fail_cuda(e);
+        if (r == SDM_GX_OK && (e = cudaEventSynchronize(e1)) != cudaSuccess) r = fail_cuda(e);
+        if (r == SDM_GX_OK && (e = cudaEventElapsedTime(&ms, e0, e1)) != cudaSuccess) r = fail_cuda(e);
+        sdm_gx_gemm_plan_destroy(pk);   // host memory only: the launches hold copies of its parameters
+        if (r != SDM_GX_OK) {
+            rc = r;
+            break;
+        }
+        const float us = ms * 1000.0f / static_cast<float>(steps);
+        if (best < 0 || us < best_us) {
+            best = k;
+            best_us = us;
+        }
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (rc != SDM_GX_OK) return rc;
+    uint32_t word = 0;
+    if ((rc = sdm_gx_device_error(&word, 0)) != SDM_GX_OK) return rc;
+    if (best < 0) return SDM_GX_E_SMEM;   // not reached: the automatic plan's configuration is among those timed
+    *flags_out = flags | static_cast<unsigned>(best + 1);
+    if (config_out != nullptr) *config_out = best;
+    if (us_out != nullptr) *us_out = best_us;
+    return SDM_GX_OK;
+}
+
 int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, int64_t ti_end, cudaStream_t stream, int pdl) {
     int rc = plan_check(plan);
     if (rc != SDM_GX_OK) return rc;

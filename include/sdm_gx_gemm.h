@@ -192,6 +192,30 @@ SDM_GX_API int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x,
                                                int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides,
                                                unsigned flags, size_t *bytes);
 
+/*
+ * Measure instead of estimate. The page picks the tile height by a rule, and the plans here pick a configuration by an
+ * estimate of the step time, which on some shapes is not the fastest. This call times every configuration of the
+ * path that a plan of this shape and layout takes, and reports the fastest. Each configuration is forced in turn
+ * (SDM_GX_FLAG_CONFIG_MASK) into a plan over the caller's buffers; the call skips those the shape, the device or the
+ * workspace does not admit, and times the rest over 2 untimed steps and then `steps` timed steps (1 .. 4096). Steps
+ * cycle over ti = 0 .. N/P - 1 and are chained with programmatic dependent launch, as sdm_gx_gemm_plan_run chains them.
+ *   d_u: a scratch buffer with the shape and strides of the real d_u. The timed steps update it in place, so pass a
+ *   copy, never the real d_u. x, d_dv, N, P, C, hd, strides, workspace: as for sdm_gx_gemm_plan_create_ws. A workspace
+ *   lets the stream configurations take part; the plan created afterwards must then have one too.
+ *   flags: base flags (SDM_GX_FLAG_GENERIC or SDM_GX_FLAG_NO_PREFETCH); a forced configuration or
+ *   SDM_GX_FLAG_TEST_STALL in them is SDM_GX_E_FLAGS.
+ *   *flags_out: flags | (index + 1) of the fastest configuration, for sdm_gx_gemm_plan_create[_ws] on buffers of
+ *   the same shape and layout. *config_out and *us_out (each nullable): its index and its time per step.
+ * Runs on `stream`, waits for it, and synchronises the device. Creating a plan for a stream configuration also
+ * synchronises the device. No device memory is allocated.
+ * Errors: those of sdm_gx_gemm_plan_create_ws; SDM_GX_E_NULL (flags_out NULL); SDM_GX_E_RANGE (steps out of range);
+ * SDM_GX_E_CUDA; SDM_GX_E_DEVICE_FAULT when the device error word is set at the end.
+ */
+SDM_GX_API int sdm_gx_gemm_autotune(float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C,
+                                    int64_t hd, const sdm_gx_strides *strides, unsigned flags, void *workspace,
+                                    size_t workspace_bytes, int steps, cudaStream_t stream, unsigned *flags_out,
+                                    int32_t *config_out, float *us_out);
+
 /* Launch step ti of a plan on `stream` (pdl as above). Errors: SDM_GX_E_PLAN (NULL / corrupt plan),
  * SDM_GX_E_PLAN_TI (ti < 0 or ti > ti_max), SDM_GX_E_PLAN_DEVICE (current device differs), SDM_GX_E_CUDA. */
 SDM_GX_API int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl);

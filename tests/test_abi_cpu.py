@@ -107,6 +107,26 @@ def test_plan_errors_without_gpu():
     L.sdm_gx_gemm_plan_destroy(ctypes.cast(junk, ctypes.c_void_p))   # not a plan: ignored
 
 
+def test_autotune_argument_errors():
+    f = L.sdm_gx_gemm_autotune
+    fo, co, us = ctypes.c_uint(7), ctypes.c_int32(-1), ctypes.c_float(0.0)
+
+    def call(flags_out=ctypes.byref(fo), steps=8, flags=0, N=8, P=2, C=16, hd=32, du=U):
+        return f(du, X, V, N, P, C, hd, None, flags, None, 0, steps, None, flags_out, ctypes.byref(co),
+                 ctypes.byref(us))
+
+    assert call(flags_out=None) == CODE["SDM_GX_E_NULL"]
+    assert call(steps=0) == CODE["SDM_GX_E_RANGE"]
+    assert call(steps=4097) == CODE["SDM_GX_E_RANGE"]
+    assert call(flags=gx.config_flag(3)) == CODE["SDM_GX_E_FLAGS"]       # a forced configuration is the output
+    assert call(flags=gx._binding.FLAG_TEST_STALL) == CODE["SDM_GX_E_FLAGS"]
+    assert call(P=0) == CODE["SDM_GX_E_RANGE"]
+    assert call(N=1) == CODE["SDM_GX_E_RANGE"]
+    assert call(C=0) == CODE["SDM_GX_E_SHAPE"]                            # the plan's own checks
+    assert call(du=0) == CODE["SDM_GX_E_NULL"]
+    assert fo.value == 7 and co.value == -1                                  # outputs untouched on error
+
+
 def test_producer_argument_errors():
     f = L.sdm_gx_producer_step
     assert f(0, V, 0, 2, 16, 32, None, 0) == CODE["SDM_GX_E_NULL"]

@@ -592,3 +592,34 @@ def test_stream_kernel_all_tile_shapes(P, C, hd):
         assert_bitwise(du.host(), want, f"stream config {k} ({info['TI']} x {info['TC']}) P={P} C={C} hd={hd}")
         assert du.guards_intact()
         gr.close()
+
+
+@pytest.mark.parametrize("case", ["ws", "no_ws", "generic"])
+def test_autotune_then_plan_is_bit_exact(case):
+    """sdm_gx_gemm_autotune times the admitted configurations on a scratch copy of d_u; a plan forced to its pick
+    gives the oracle's bits, and the tuning leaves x, d_dv and the real d_u alone. 160 x 64 x 128 is a shape where
+    the plan's estimate is not the fastest; the generic case (rows padded to 129 floats) tunes the generic path."""
+    P, C, hd = (160, 64, 128) if case != "generic" else (16, 48, 100)
+    w = synth.Workload("autotune", 61, T=2, P=P, C=C, hd=hd)
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    row_pad = 29 if case == "generic" else 0
+    du, dx, dv = _dev(inp, row_pad=row_pad)
+    scratch = DevArray(inp["d_u"], 0, row_pad)
+    res = gx.autotune(scratch.t, dx.t, dv.t, w.P, steps=10, workspace=(case == "ws"))
+    torch.cuda.synchronize()
+    path = 0 if case == "generic" else 1
+    assert 0 <= res["config"] < gx.num_configs(path) and res["us"] > 0.0
+    assert res["flags"] == gx.config_flag(res["config"])
+    if case == "no_ws":
+        assert gx.config_info(1, res["config"])["kind"] != "stream"
+    assert_bitwise(du.host(), inp["d_u"], "autotune touched d_u")
+    _check_untouched(dx, dv, inp, "autotune")
+    assert scratch.guards_intact() and dx.guards_intact() and dv.guards_intact()
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=res["flags"], workspace=(case == "ws"))
+    g = pl.geometry()
+    assert (g["path"], g["config"]) == (path, res["config"])
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"autotuned plan ({case})")
+    assert du.guards_intact()
