@@ -1,7 +1,8 @@
 // The generic kernel of the gx_gemm step update (any element strides, 4-byte alignment, any C <= 256 and hd), and
 // the synthetic producer kernel of the chained workload. sm_103a.
 //
-// Generic kernel: CTAs of 256 threads loop over tiles of TI rows x 64 columns of one chunk (grid <= resident slots).
+// Generic kernel: CTAs of 256 threads loop over tiles of TI rows x 64 columns of one chunk (grid <= resident slots);
+// a large-tile variant (below) serves steps whose 128 x 64 tiles fill the SMs.
 // Thread (tx, ty) of a 16 x 16 layout owns rows i0 + ty + 16 r (r < TI / 16) and columns c0 + tx + 16 q (q < 4), so
 // global reads and writes of d_u are coalesced along c. The j range is staged KB = 32 rows at a time into shared
 // memory (xs[KB][TI] from x[n, j, i], ds[KB][64] from d_dv[n, j, c], zero past C / hd) with plain loads, and every
@@ -119,15 +120,138 @@ ConfigInfo generic_info() {
     return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32, 40, 0};
 }
 
+// Large-tile generic kernel, for steps whose 128 x 64 tiles fill the SMs. CTAs of 256 threads loop over 128 x 64
+// tiles. Warp w owns rows 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31 in lanes of 4 x 8; a thread owns rows
+// ro .. ro + 3 and ro + 16 .. ro + 19 (ro = 32 (w % 4) + 4 (lane / 8)) of columns co .. co + 3 (co = 32 (w / 4) +
+// 4 (lane % 8)), as in the TMA kernel's consumers, and runs its 8 x 4 chains with packed FMAs along rows (lane by lane
+// the same fused multiply-add as fmaf). j is staged 32 rows at a time into one of two shared buffers with plain 4-byte
+// loads (any strides, zero fill past C / hd): the next block is read into registers while the current one is used,
+// then stored to the other buffer. d_u is read in the epilogue and written as d_u + acc; every access comes after the
+// dependency wait.
+constexpr int kBigTI = 128, kBigTC = 64, kBigKB = 32, kBigNT = 256;
+constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread stages per block of j (rows xj + 2k)
+constexpr int kBigDE = kBigKB * kBigTC / kBigNT;   // d_dv elements (rows dj + 4k)
+
+__device__ __forceinline__ void big_chain_j(const float *xb, const float *db, int jj, int ro, int co,
+                                            float (&acc)[8][4]) {
+    float a[8], b[4];
+    dev::Vec<4>::load(xb + jj * kBigTI + ro, a);
+    dev::Vec<4>::load(xb + jj * kBigTI + ro + 16, a + 4);
+    dev::Vec<4>::load(db + jj * kBigTC + co, b);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int r = 0; r < 8; r += 2) dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
+    }
+}
+
+__global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const GenericParams p) {
+    __shared__ __align__(16) float xs[2][kBigKB][kBigTI];
+    __shared__ __align__(16) float ds[2][kBigKB][kBigTC];
+    const int tid = static_cast<int>(threadIdx.x);
+    const int warp = tid / 32, lane = tid % 32;
+    const int ro = (warp % 4) * 32 + (lane / 8) * 4;
+    const int co = (warp / 4) * 32 + (lane % 8) * 4;
+    const int xi = tid % kBigTI, xj = tid / kBigTI;
+    const int di = tid % kBigTC, dj = tid / kBigTC;
+    const int per_chunk = p.nib * p.ncb;
+    const int nkb = (p.C + kBigKB - 1) / kBigKB;
+    dev::grid_dependency_wait();
+    dev::launch_dependents();
+    for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x)) {
+        const int pp = t / per_chunk;
+        const int rem = t - pp * per_chunk;
+        const int ib = rem / p.ncb;
+        const int cb = rem - ib * p.ncb;
+        const int64_t n = p.n_base + pp;
+        const int i0 = ib * kBigTI, c0 = cb * kBigTC;
+        const float *xn = p.x + n * p.x_sn;
+        const float *dvn = p.dv + n * p.dv_sn;
+        float *dun = p.du + n * p.du_sn;
+        float px[kBigXE], pd[kBigDE];
+        auto fetch = [&](int j0) {
+#pragma unroll
+            for (int k = 0; k < kBigXE; ++k) {
+                const int j = j0 + xj + 2 * k, i = i0 + xi;
+                px[k] = (j < p.C && i < p.C) ? xn[static_cast<int64_t>(j) * p.x_sj + i] : 0.0f;
+            }
+#pragma unroll
+            for (int k = 0; k < kBigDE; ++k) {
+                const int j = j0 + dj + 4 * k, c = c0 + di;
+                pd[k] = (j < p.C && c < p.hd) ? dvn[static_cast<int64_t>(j) * p.dv_sj + c] : 0.0f;
+            }
+        };
+        auto put = [&](int b) {
+#pragma unroll
+            for (int k = 0; k < kBigXE; ++k) xs[b][xj + 2 * k][xi] = px[k];
+#pragma unroll
+            for (int k = 0; k < kBigDE; ++k) ds[b][dj + 4 * k][di] = pd[k];
+        };
+        float acc[8][4];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;   // +0: the chain's start value
+        }
+        fetch(0);
+        put(0);
+        __syncthreads();
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int b = kb & 1;
+            if (kb + 1 < nkb) fetch((kb + 1) * kBigKB);
+            const float *xb = &xs[b][0][0];
+            const float *db = &ds[b][0][0];
+            const int nj = p.C - kb * kBigKB < kBigKB ? p.C - kb * kBigKB : kBigKB;
+            if (nj == kBigKB) {
+#pragma unroll 8
+                for (int jj = 0; jj < kBigKB; ++jj) big_chain_j(xb, db, jj, ro, co, acc);
+            } else {
+#pragma unroll 1
+                for (int jj = 0; jj < nj; ++jj) big_chain_j(xb, db, jj, ro, co, acc);
+            }
+            if (kb + 1 < nkb) put(b ^ 1);   // the other buffer: every thread left it at the previous barrier
+            __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const int i = i0 + ro + (r / 4) * 16 + (r % 4);
+            if (i >= p.C) continue;
+            float *row = dun + static_cast<int64_t>(i) * p.du_si;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int cc = c0 + co + c;
+                if (cc < p.hd) row[cc] = __fadd_rn(row[cc], acc[r][c]);
+            }
+        }
+    }
+}
+
+cudaError_t launch_generic_big(const GenericParams &p, int grid, cudaStream_t st, int pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kBigNT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gx_generic_big_kernel, p);
+}
+
 struct GEntry {
     ConfigInfo info;
     const void *fn;
     cudaError_t (*launch)(const GenericParams &, int, cudaStream_t, int);
 };
+// the large-tile kernel stays last (the host's choice relies on it)
 const GEntry kGen[] = {
     {generic_info<16>(), reinterpret_cast<const void *>(&gx_generic_kernel<16>), &launch_generic<16>},
     {generic_info<32>(), reinterpret_cast<const void *>(&gx_generic_kernel<32>), &launch_generic<32>},
     {generic_info<64>(), reinterpret_cast<const void *>(&gx_generic_kernel<64>), &launch_generic<64>},
+    {ConfigInfo{kBigTI, kBigTC, kBigKB, 2, kBigNT, 2 * (kBigKB * kBigTI + kBigKB * kBigTC) * 4, 8, 4, kBigNT / 32, 50, 0},
+     reinterpret_cast<const void *>(&gx_generic_big_kernel), &launch_generic_big},
 };
 
 // ---- synthetic producer: d_dv[base + e] = +-S[base + e], e < count --------------------------------------------------

@@ -321,12 +321,17 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
 
 int choose_generic_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
     if (forced >= 0) return forced;
-    for (int k = 0; k < generic_num_configs(); ++k) {
+    // a step whose 128 x 64 tiles fill the SMs runs the large-tile kernel (the last configuration); smaller steps the
+    // smallest tile that still fits one wave of resident CTAs (latency-bound)
+    const int big = generic_num_configs() - 1;
+    const ConfigInfo &cg = generic_config(big);
+    if (P * ((C + cg.TI - 1) / cg.TI) * ((hd + cg.TC - 1) / cg.TC) >= d.sms) return big;
+    for (int k = 0; k < big; ++k) {
         const ConfigInfo &ci = generic_config(k);
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
         if (tiles <= static_cast<int64_t>(d.sms) * std::max(1, d.gen_occ[k])) return k;
     }
-    return generic_num_configs() - 1;
+    return big - 1;
 }
 
 CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t rows, int64_t chunks, int64_t sr,

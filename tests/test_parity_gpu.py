@@ -113,7 +113,14 @@ def test_every_tma_config_ragged(config):
     _check_untouched(dx, dv, inp, f"tma config {config}")
 
 
-@pytest.mark.parametrize("config", [0, 1, 2])
+GENERIC_CONFIGS = [0, 1, 2, 3]
+
+
+def test_generic_menu_covered():
+    assert gx.num_configs(0) == len(GENERIC_CONFIGS), "every generic configuration must be in GENERIC_CONFIGS"
+
+
+@pytest.mark.parametrize("config", GENERIC_CONFIGS)
 @pytest.mark.parametrize("shape", [(100, 76), (48, 99), (256, 3), (1, 1), (7, 130)])
 def test_every_generic_config(config, shape):
     C, hd = shape
@@ -651,3 +658,29 @@ def test_latency_rule_prefers_small_tiles(shape):
     pl.run(pdl=True)
     torch.cuda.synchronize()
     assert_bitwise(du.host(), want, f"latency rule {shape}")
+
+
+@pytest.mark.parametrize("layout", ["ld129", "offset4"])
+def test_generic_large_tile_kernel(layout):
+    """The generic path's large-tile kernel (128 x 64 tiles, packed FMAs, register-prefetched double-buffered staging)
+    on layouts TMA cannot describe: rows of 129 floats, and bases 4 bytes past a 16-byte boundary. 80 chunks of
+    C = 130, hd = 100 span several tiles per CTA with ragged rows, columns and j; the plan picks the kernel itself
+    once its tiles fill the SMs (here forced, then checked on a filling step)."""
+    w = synth.Workload("generic_big", 63, T=2, P=80, C=130, hd=100, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    offset, row_pad = (0, 29) if layout == "ld129" else (1, 0)
+    du, dx, dv = _dev(inp, offset=offset, row_pad=row_pad)
+    big = gx.num_configs(0) - 1
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(big))
+    g = pl.geometry()
+    assert (g["path"], g["config"], g["TI"], g["TC"]) == (0, big, 128, 64)
+    pl.run(w.T - 1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"generic large-tile kernel ({layout})")
+    assert du.guards_intact() and dx.guards_intact() and dv.guards_intact()
+    _check_untouched(dx, dv, inp, f"generic large-tile kernel ({layout})")
+    # a step whose 128 x 64 tiles fill the SMs takes it without being asked
+    assert 2 * w.P * 2 >= g["sms"]
+    auto = gx.Plan(du.t, dx.t, dv.t, w.P).geometry()
+    assert (auto["path"], auto["config"]) == (0, big)
