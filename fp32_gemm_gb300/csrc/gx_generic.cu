@@ -124,12 +124,12 @@ ConfigInfo generic_info() {
 // tiles. Warp w owns rows 32 (w % 4) .. + 31 and columns 32 (w / 4) .. + 31 in lanes of 4 x 8; a thread owns rows
 // ro .. ro + 3 and ro + 16 .. ro + 19 (ro = 32 (w % 4) + 4 (lane / 8)) of columns co .. co + 3 (co = 32 (w / 4) +
 // 4 (lane % 8)), as in the TMA kernel's consumers, and runs its 8 x 4 chains with packed FMAs along rows (lane by lane
-// the same fused multiply-add as fmaf). j is staged 32 rows at a time into one of two shared buffers with plain 4-byte
-// loads (any strides, zero fill past C / hd): the next block is read into registers while the current one is used,
-// then stored to the other buffer. d_u is read in the epilogue and written as d_u + acc; every access comes after the
-// dependency wait.
+// the same fused multiply-add as fmaf). j is staged 32 rows at a time into one of two shared buffers by 4-byte
+// asynchronous copies (cp.async: any strides, zero fill past C / hd); the copies of the next block, of this tile or of
+// the CTA's next tile, are in flight while the current block is used. d_u is prefetched into L2 when a tile starts, read
+// in the epilogue and written as d_u + acc; every access comes after the dependency wait.
 constexpr int kBigTI = 128, kBigTC = 64, kBigKB = 32, kBigNT = 256;
-constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread stages per block of j (rows xj + 2k)
+constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread copies per block of j (rows xj + 2k)
 constexpr int kBigDE = kBigKB * kBigTC / kBigNT;   // d_dv elements (rows dj + 4k)
 
 __device__ __forceinline__ void big_chain_j(const float *xb, const float *db, int jj, int ro, int co,
@@ -156,51 +156,72 @@ __global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const Generic
     const int di = tid % kBigTC, dj = tid / kBigTC;
     const int per_chunk = p.nib * p.ncb;
     const int nkb = (p.C + kBigKB - 1) / kBigKB;
+    const int stride = static_cast<int>(gridDim.x);
     dev::grid_dependency_wait();
     dev::launch_dependents();
-    for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x)) {
+    const uint32_t xs_s = dev::smem_addr(&xs[0][0][0]);
+    const uint32_t ds_s = dev::smem_addr(&ds[0][0][0]);
+    // this thread's copies of block kb (rows j0 .. j0 + 31) of tile t into buffer b, as one copy group
+    auto issue = [&](int t, int kb, int b) {
         const int pp = t / per_chunk;
         const int rem = t - pp * per_chunk;
         const int ib = rem / p.ncb;
-        const int cb = rem - ib * p.ncb;
         const int64_t n = p.n_base + pp;
-        const int i0 = ib * kBigTI, c0 = cb * kBigTC;
+        const int i0 = ib * kBigTI, c0 = (rem - ib * p.ncb) * kBigTC;
         const float *xn = p.x + n * p.x_sn;
         const float *dvn = p.dv + n * p.dv_sn;
+        const int j0 = kb * kBigKB;
+#pragma unroll
+        for (int k = 0; k < kBigXE; ++k) {
+            const int j = j0 + xj + 2 * k, i = i0 + xi;
+            const bool ok = j < p.C && i < p.C;
+            dev::cp_async_4(xs_s + static_cast<uint32_t>(((b * kBigKB + xj + 2 * k) * kBigTI + xi) * 4),
+                            ok ? xn + static_cast<int64_t>(j) * p.x_sj + i : xn, ok ? 4u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < kBigDE; ++k) {
+            const int j = j0 + dj + 4 * k, c = c0 + di;
+            const bool ok = j < p.C && c < p.hd;
+            dev::cp_async_4(ds_s + static_cast<uint32_t>(((b * kBigKB + dj + 4 * k) * kBigTC + di) * 4),
+                            ok ? dvn + static_cast<int64_t>(j) * p.dv_sj + c : dvn, ok ? 4u : 0u);
+        }
+        dev::cp_async_commit();
+    };
+    int s = 0;   // blocks this CTA has used so far; block s sits in buffer s & 1
+    if (static_cast<int>(blockIdx.x) < p.ntiles) issue(static_cast<int>(blockIdx.x), 0, 0);
+    for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += stride) {
+        const int pp = t / per_chunk;
+        const int rem = t - pp * per_chunk;
+        const int ib = rem / p.ncb;
+        const int64_t n = p.n_base + pp;
+        const int i0 = ib * kBigTI, c0 = (rem - ib * p.ncb) * kBigTC;
         float *dun = p.du + n * p.du_sn;
-        float px[kBigXE], pd[kBigDE];
-        auto fetch = [&](int j0) {
+        if (c0 + co < p.hd) {   // the epilogue's d_u rows into L2 while the chain runs
 #pragma unroll
-            for (int k = 0; k < kBigXE; ++k) {
-                const int j = j0 + xj + 2 * k, i = i0 + xi;
-                px[k] = (j < p.C && i < p.C) ? xn[static_cast<int64_t>(j) * p.x_sj + i] : 0.0f;
+            for (int r = 0; r < 8; ++r) {
+                const int i = i0 + ro + (r / 4) * 16 + (r % 4);
+                if (i < p.C) dev::prefetch_l2(dun + static_cast<int64_t>(i) * p.du_si + c0 + co);
             }
-#pragma unroll
-            for (int k = 0; k < kBigDE; ++k) {
-                const int j = j0 + dj + 4 * k, c = c0 + di;
-                pd[k] = (j < p.C && c < p.hd) ? dvn[static_cast<int64_t>(j) * p.dv_sj + c] : 0.0f;
-            }
-        };
-        auto put = [&](int b) {
-#pragma unroll
-            for (int k = 0; k < kBigXE; ++k) xs[b][xj + 2 * k][xi] = px[k];
-#pragma unroll
-            for (int k = 0; k < kBigDE; ++k) ds[b][dj + 4 * k][di] = pd[k];
-        };
+        }
         float acc[8][4];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;   // +0: the chain's start value
         }
-        fetch(0);
-        put(0);
-        __syncthreads();
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int b = kb & 1;
-            if (kb + 1 < nkb) fetch((kb + 1) * kBigKB);
-            const float *xb = &xs[b][0][0];
-            const float *db = &ds[b][0][0];
+        for (int kb = 0; kb < nkb; ++kb, ++s) {
+            // the next block (of this tile, else block 0 of the CTA's next tile) goes into the other buffer, which
+            // every thread left at the barrier that ended the previous block
+            const int nt = kb + 1 < nkb ? t : t + stride;
+            if (nt < p.ntiles) {
+                issue(nt, kb + 1 < nkb ? kb + 1 : 0, (s + 1) & 1);
+                dev::cp_async_wait<1>();
+            } else {
+                dev::cp_async_wait<0>();
+            }
+            __syncthreads();   // every thread's copies of block s have landed
+            const float *xb = &xs[s & 1][0][0];
+            const float *db = &ds[s & 1][0][0];
             const int nj = p.C - kb * kBigKB < kBigKB ? p.C - kb * kBigKB : kBigKB;
             if (nj == kBigKB) {
 #pragma unroll 8
@@ -209,8 +230,7 @@ __global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const Generic
 #pragma unroll 1
                 for (int jj = 0; jj < nj; ++jj) big_chain_j(xb, db, jj, ro, co, acc);
             }
-            if (kb + 1 < nkb) put(b ^ 1);   // the other buffer: every thread left it at the previous barrier
-            __syncthreads();
+            __syncthreads();   // buffer s & 1 is free for block s + 2
         }
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
