@@ -108,19 +108,6 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
                  : "memory");
 }
 // waits until every bulk group this thread committed has completed (its writes performed)
-// 4-byte asynchronous copy global -> shared (cached in L1); src_bytes = 0 writes a zero and reads nothing
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const float *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most N of this thread's copy groups are still in flight
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void *ptr) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
-}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ---- flags between CTAs (global memory, GPU scope) ---------------------------------------------------------------------

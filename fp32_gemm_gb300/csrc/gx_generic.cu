@@ -128,6 +128,19 @@ ConfigInfo generic_info() {
 // asynchronous copies (cp.async: any strides, zero fill past C / hd); the copies of the next block, of this tile or of
 // the CTA's next tile, are in flight while the current block is used. d_u is prefetched into L2 when a tile starts, read
 // in the epilogue and written as d_u + acc; every access comes after the dependency wait.
+// 4-byte asynchronous copy global -> shared (cached in L1); src_bytes = 0 writes a zero and reads nothing
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const float *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's copy groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
+}
 constexpr int kBigTI = 128, kBigTC = 64, kBigKB = 32, kBigNT = 256;
 constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread copies per block of j (rows xj + 2k)
 constexpr int kBigDE = kBigKB * kBigTC / kBigNT;   // d_dv elements (rows dj + 4k)
@@ -175,17 +188,17 @@ __global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const Generic
         for (int k = 0; k < kBigXE; ++k) {
             const int j = j0 + xj + 2 * k, i = i0 + xi;
             const bool ok = j < p.C && i < p.C;
-            dev::cp_async_4(xs_s + static_cast<uint32_t>(((b * kBigKB + xj + 2 * k) * kBigTI + xi) * 4),
+            cp_async_4(xs_s + static_cast<uint32_t>(((b * kBigKB + xj + 2 * k) * kBigTI + xi) * 4),
                             ok ? xn + static_cast<int64_t>(j) * p.x_sj + i : xn, ok ? 4u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < kBigDE; ++k) {
             const int j = j0 + dj + 4 * k, c = c0 + di;
             const bool ok = j < p.C && c < p.hd;
-            dev::cp_async_4(ds_s + static_cast<uint32_t>(((b * kBigKB + dj + 4 * k) * kBigTC + di) * 4),
+            cp_async_4(ds_s + static_cast<uint32_t>(((b * kBigKB + dj + 4 * k) * kBigTC + di) * 4),
                             ok ? dvn + static_cast<int64_t>(j) * p.dv_sj + c : dvn, ok ? 4u : 0u);
         }
-        dev::cp_async_commit();
+        cp_async_commit();
     };
     int s = 0;   // blocks this CTA has used so far; block s sits in buffer s & 1
     if (static_cast<int>(blockIdx.x) < p.ntiles) issue(static_cast<int>(blockIdx.x), 0, 0);
@@ -200,7 +213,7 @@ __global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const Generic
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = i0 + ro + (r / 4) * 16 + (r % 4);
-                if (i < p.C) dev::prefetch_l2(dun + static_cast<int64_t>(i) * p.du_si + c0 + co);
+                if (i < p.C) prefetch_l2(dun + static_cast<int64_t>(i) * p.du_si + c0 + co);
             }
         }
         float acc[8][4];
@@ -215,9 +228,9 @@ __global__ void __launch_bounds__(kBigNT, 2) gx_generic_big_kernel(const Generic
             const int nt = kb + 1 < nkb ? t : t + stride;
             if (nt < p.ntiles) {
                 issue(nt, kb + 1 < nkb ? kb + 1 : 0, (s + 1) & 1);
-                dev::cp_async_wait<1>();
+                cp_async_wait<1>();
             } else {
-                dev::cp_async_wait<0>();
+                cp_async_wait<0>();
             }
             __syncthreads();   // every thread's copies of block s have landed
             const float *xb = &xs[s & 1][0][0];
