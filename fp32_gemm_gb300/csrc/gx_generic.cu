@@ -283,7 +283,7 @@ const GEntry kGen[] = {
     {generic_info<16>(), reinterpret_cast<const void *>(&gx_generic_kernel<16>), &launch_generic<16>},
     {generic_info<32>(), reinterpret_cast<const void *>(&gx_generic_kernel<32>), &launch_generic<32>},
     {generic_info<64>(), reinterpret_cast<const void *>(&gx_generic_kernel<64>), &launch_generic<64>},
-    {ConfigInfo{kBigTI, kBigTC, kBigKB, 2, kBigNT, 2 * (kBigKB * kBigTI + kBigKB * kBigTC) * 4, 8, 4, kBigNT / 32, 50, 0},
+    {ConfigInfo{kBigTI, kBigTC, kBigKB, 2, kBigNT, 0, 8, 4, kBigNT / 32, 50, 0},   // 48 KB of static shared memory
      reinterpret_cast<const void *>(&gx_generic_big_kernel), &launch_generic_big},
 };
 

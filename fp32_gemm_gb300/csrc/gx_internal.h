@@ -116,7 +116,7 @@ const ConfigInfo &tma_config(int k);
 const void *tma_kernel(int k);
 cudaError_t tma_launch(int k, const TmaParams &p, int grid, cudaStream_t st, int pdl);
 
-// generic path (config k: 16, 32, 64 rows per tile)
+// generic path (configs 0..2: 16, 32, 64 x 64 tiles; 3, the last: the 128 x 64 large-tile kernel)
 int generic_num_configs();
 const ConfigInfo &generic_config(int k);
 const void *generic_kernel(int k);

@@ -287,7 +287,8 @@ SDM_GX_API int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int
                          cudaStream_t stream, int pdl);
 
 /* Registers per thread, local (spill) bytes, static shared bytes and max threads per block of a kernel:
- * path 0 = generic (config 0..2 = 16/32/64 rows), path 1 = TMA (config index as in sdm_gx_geom). out[4]. */
+ * path 0 = generic (config 0..2 = 16/32/64 x 64 tiles, 3 = the 128 x 64 large-tile kernel), path 1 = TMA (config
+ * index as in sdm_gx_geom). out[4]. */
 SDM_GX_API int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]);
 
 /* Static description of configuration `config` of a path (for sweeps and tests): out[0..7] = TI, TC, KB, stages,
