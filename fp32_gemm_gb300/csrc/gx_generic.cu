@@ -128,6 +128,10 @@ ConfigInfo generic_info() {
 // asynchronous copies (cp.async: any strides, zero fill past C / hd); the copies of the next block, of this tile or of
 // the CTA's next tile, are in flight while the current block is used. d_u is prefetched into L2 when a tile starts, read
 // in the epilogue and written as d_u + acc; every access comes after the dependency wait.
+constexpr int kBigTI = 128, kBigTC = 64, kBigKB = 32, kBigNT = 256;
+constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread copies per block of j (rows xj + 2k)
+constexpr int kBigDE = kBigKB * kBigTC / kBigNT;   // d_dv elements (rows dj + 4k)
+
 // 4-byte asynchronous copy global -> shared (cached in L1); src_bytes = 0 writes a zero and reads nothing
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const float *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -141,9 +145,6 @@ __device__ __forceinline__ void cp_async_wait() {
 __device__ __forceinline__ void prefetch_l2(const void *ptr) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
 }
-constexpr int kBigTI = 128, kBigTC = 64, kBigKB = 32, kBigNT = 256;
-constexpr int kBigXE = kBigKB * kBigTI / kBigNT;   // x elements a thread copies per block of j (rows xj + 2k)
-constexpr int kBigDE = kBigKB * kBigTC / kBigNT;   // d_dv elements (rows dj + 4k)
 
 __device__ __forceinline__ void big_chain_j(const float *xb, const float *db, int jj, int ro, int co,
                                             float (&acc)[8][4]) {
