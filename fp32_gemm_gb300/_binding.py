@@ -92,6 +92,9 @@ SIGNATURES = {
                              [ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_kernel_attrs": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)]),
     "sdm_gx_gemm_num_configs": (ctypes.c_int, [ctypes.c_int32]),
+    "sdm_gx_gemm_choose_config": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                                 ctypes.c_int32, ctypes.c_int32] + [ctypes.c_int64] * 3 +
+                                  [ctypes.c_size_t]),
     "sdm_gx_gemm_config_info": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "sdm_gx_gemm_stream_piece": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                 ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
@@ -395,6 +398,17 @@ def config_info(path: int, config: int) -> dict:
     _check(_lib.sdm_gx_gemm_config_info(int(path), int(config), out), "sdm_gx_gemm_config_info")
     return {"TI": out[0], "TC": out[1], "KB": out[2], "stages": out[3], "threads": out[4], "smem": out[5],
             "kind": CONFIG_KINDS.get(out[6], str(out[6])), "consumer_warps": out[7]}
+
+
+def choose_config(path: int, sms: int, occ, P: int, C: int, hd: int, ws_bytes: int = 0, slab_ok: bool = True) -> int:
+    """sdm_gx_gemm_choose_config: the configuration a plan would choose on a described device (SM count, resident
+    CTAs per SM of every configuration of the path, workspace bytes); no GPU needed."""
+    arr = (ctypes.c_int32 * len(occ))(*[int(v) for v in occ])
+    k = _lib.sdm_gx_gemm_choose_config(int(path), int(sms), arr, len(occ), int(bool(slab_ok)), int(P), int(C), int(hd),
+                                       int(ws_bytes))
+    if k < 0:
+        raise GxGemmError(k, "sdm_gx_gemm_choose_config")
+    return int(k)
 
 
 def stream_pieces(ntiles: int, C: int, G: int, b: int) -> list[tuple[int, int, int, int]]:

@@ -1136,6 +1136,25 @@ int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, in
     return SDM_GX_OK;
 }
 
+int sdm_gx_gemm_choose_config(int32_t path, int32_t sms, const int32_t *occ, int32_t n_occ, int32_t slab_ok,
+                              int64_t P, int64_t C, int64_t hd, size_t ws_bytes) {
+    if (occ == nullptr) return SDM_GX_E_NULL;
+    if (path != 0 && path != 1) return SDM_GX_E_FLAGS;
+    if (C < 1 || C > 256 || hd < 1 || hd >= (int64_t(1) << 20)) return SDM_GX_E_SHAPE;
+    const int nk = path == 1 ? tma_num_configs() : generic_num_configs();
+    if (sms < 1 || sms > 4096 || n_occ != nk || P < 1 || P >= kTwo31) return SDM_GX_E_RANGE;
+    DevState d;
+    d.sms = sms;
+    d.slab_ok = slab_ok != 0;
+    for (int k = 0; k < nk; ++k) {
+        if (occ[k] < 0) return SDM_GX_E_RANGE;
+        (path == 1 ? d.tma_occ : d.gen_occ)[k] = occ[k];
+    }
+    if (path == 0) return choose_generic_config(d, P, C, hd, -1);
+    const int k = choose_tma_config(d, P, C, hd, -1, ws_bytes, 1 << 30);
+    return k >= 0 ? k : SDM_GX_E_SMEM;
+}
+
 int sdm_gx_gemm_num_configs(int32_t path) {
     if (path == 1) return tma_num_configs();
     if (path == 0) return generic_num_configs();

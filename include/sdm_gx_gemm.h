@@ -305,6 +305,16 @@ SDM_GX_API int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out
  * continuing CTA b - 1's accumulators) and returns 0. SDM_GX_E_RANGE for arguments outside those bounds. */
 SDM_GX_API int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, int32_t q, int32_t out[4]);
 
+/* The configuration a plan would choose, for a DESCRIBED device: the same rule as sdm_gx_gemm_plan_create, on the
+ * SM count `sms`, the resident CTAs per SM of every configuration of `path` (occ[k], n_occ entries =
+ * sdm_gx_gemm_num_configs(path)), whether the slab kernel's 4-D x view is available (slab_ok), and a plan workspace
+ * of ws_bytes (0: none). Makes no CUDA call (a diagnostic for tests and tools; a device's own values come from
+ * sdm_gx_gemm_geometry). Returns the configuration's index (>= 0), or SDM_GX_E_NULL (occ NULL), SDM_GX_E_FLAGS
+ * (path not 0 / 1), SDM_GX_E_SHAPE (C or hd out of range), SDM_GX_E_RANGE (sms outside [1, 4096], n_occ wrong,
+ * a negative occ, P outside [1, 2^31)), SDM_GX_E_SMEM (no configuration is usable). */
+SDM_GX_API int sdm_gx_gemm_choose_config(int32_t path, int32_t sms, const int32_t *occ, int32_t n_occ, int32_t slab_ok,
+                                         int64_t P, int64_t C, int64_t hd, size_t ws_bytes);
+
 /* Number of tile configurations of a path (for sweeps and tests). */
 SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
 

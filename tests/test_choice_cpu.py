@@ -1,0 +1,84 @@
+"""The plan's configuration choice on a described GB300-like device, without a GPU (sdm_gx_gemm_choose_config runs the
+same host rule as plan creation). The device: 152 SMs; resident CTAs per SM of every TMA configuration as their
+registers, threads and shared memory allow (1 for the 128 x 128 tiles and the one-CTA stream configuration, 2 for the
+64-128-row tiles, 4 for 32 x 64 and 16 x 64, 10 for the one-warp tiles). The expected picks are the configurations
+measured fastest on a GB300 for these shapes."""
+
+import pytest
+
+gx = pytest.importorskip("fp32_gemm_gb300")
+
+SMS = 152
+TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2]
+GEN_OCC = [6, 6, 6, 2]
+WS = 64 << 20   # a plan workspace large enough for every stream configuration
+
+
+def pick(P, C, hd, ws=WS, path=1):
+    occ = TMA_OCC if path == 1 else GEN_OCC
+    return gx.choose_config(path, SMS, occ, P, C, hd, ws_bytes=ws)
+
+
+def info(k):
+    return gx.config_info(1, k)
+
+
+def test_description_matches_the_menu():
+    assert gx.num_configs(1) == len(TMA_OCC) and gx.num_configs(0) == len(GEN_OCC)
+
+
+def test_large_step_takes_the_stream_kernel_with_a_workspace():
+    k = pick(256, 128, 128)
+    assert info(k)["kind"] == "stream" and (info(k)["TI"], info(k)["TC"]) == (128, 128)
+    k0 = pick(256, 128, 128, ws=0)   # without a workspace: the 128 x 128 tile kernel
+    assert info(k0)["kind"] == "tile" and (info(k0)["TI"], info(k0)["TC"], info(k0)["consumer_warps"]) == (128, 128, 16)
+
+
+@pytest.mark.parametrize("shape,tile", [((32, 64, 128), (32, 64)),    # pdl_chain: 128 tiles of 32 x 64
+                                        ((8, 64, 64), (8, 32)),       # producer_chain: 128 tiles of 8 x 32
+                                        ((2, 16, 32), (8, 32)),       # tiny
+                                        ((4, 48, 100), (8, 32))])     # edge, hd = 100
+def test_latency_bound_steps_fill_one_wave_with_the_most_tiles(shape, tile):
+    k = pick(*shape)
+    assert (info(k)["TI"], info(k)["TC"]) == tile
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 128), (48, 64, 128), (72, 64, 96), (100, 32, 64)])
+def test_ties_go_to_the_smallest_tile(shape):
+    """Among configurations with equally many tiles in one wave the smallest tile wins (rows and columns past C and hd
+    cost time): never 128 x 64 on C = 64 or 128 x 128 on C = 32."""
+    P, C, hd = shape
+    k = pick(*shape)
+    tiles = lambda j: P * -(-C // info(j)["TI"]) * -(-hd // info(j)["TC"])
+    same = [j for j in range(len(TMA_OCC)) if info(j)["kind"] == "tile" and tiles(j) == tiles(k)]
+    assert tiles(k) <= SMS
+    assert info(k)["TI"] * info(k)["TC"] == min(info(j)["TI"] * info(j)["TC"] for j in same)
+    assert info(k)["TI"] <= max(C, 32)
+
+
+def test_generic_path_large_tile_kernel_for_filling_steps():
+    assert pick(256, 128, 128, path=0) == len(GEN_OCC) - 1   # 512 tiles of 128 x 64: the large-tile kernel
+    assert pick(4, 48, 99, path=0) == 0                      # 4 chunks: 16-row tiles in one wave
+    # 70 x 100 x 100: 140 tiles of 128 x 64 do not fill 152 SMs; 980 16-row tiles exceed one wave of 152 x 6 resident
+    # CTAs, 560 32-row tiles fit it
+    assert pick(70, 100, 100, path=0) == 1
+    assert pick(40, 100, 100, path=0) == 0                   # 560 16-row tiles fit one wave
+
+
+def test_argument_errors():
+    codes = gx._binding.CODE
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.choose_config(1, 0, TMA_OCC, 8, 64, 64)
+    assert e.value.status == codes["SDM_GX_E_RANGE"]
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.choose_config(1, SMS, TMA_OCC[:-1], 8, 64, 64)
+    assert e.value.status == codes["SDM_GX_E_RANGE"]
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.choose_config(2, SMS, TMA_OCC, 8, 64, 64)
+    assert e.value.status == codes["SDM_GX_E_FLAGS"]
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.choose_config(1, SMS, TMA_OCC, 8, 0, 64)
+    assert e.value.status == codes["SDM_GX_E_SHAPE"]
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.choose_config(1, SMS, [0] * len(TMA_OCC), 8, 64, 64)   # nothing resident: nothing usable
+    assert e.value.status == codes["SDM_GX_E_SMEM"]
