@@ -1,8 +1,8 @@
 """The plan's configuration choice on a described GB300-like device, without a GPU (sdm_gx_gemm_choose_config runs the
-same host rule as plan creation). The device: 152 SMs; resident CTAs per SM of every TMA configuration as their
-registers, threads and shared memory allow (1 for the 128 x 128 tiles and the one-CTA stream configuration, 2 for the
-64-128-row tiles, 4 for 32 x 64 and 16 x 64, 10 for the one-warp tiles). The expected picks are the configurations
-measured fastest on a GB300 for these shapes."""
+same host rule as plan creation). The device: 152 SMs and the resident CTAs per SM of every configuration, both as a
+GB300 reports them through plan geometry (1 for the 128 x 128 tiles and the one-CTA stream configuration, 2 for the
+64-128-row tiles, 4 for 32 x 64 and 16 x 64, 10 for the one-warp tiles; generic 6, 4, 2, 2). The expected picks are
+the configurations measured fastest on a GB300 for these shapes."""
 
 import pytest
 
@@ -10,7 +10,7 @@ gx = pytest.importorskip("fp32_gemm_gb300")
 
 SMS = 152
 TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2]
-GEN_OCC = [6, 6, 6, 2]
+GEN_OCC = [6, 4, 2, 2]
 WS = 64 << 20   # a plan workspace large enough for every stream configuration
 
 
@@ -60,7 +60,7 @@ def test_generic_path_large_tile_kernel_for_filling_steps():
     assert pick(256, 128, 128, path=0) == len(GEN_OCC) - 1   # 512 tiles of 128 x 64: the large-tile kernel
     assert pick(4, 48, 99, path=0) == 0                      # 4 chunks: 16-row tiles in one wave
     # 70 x 100 x 100: 140 tiles of 128 x 64 do not fill 152 SMs; 980 16-row tiles exceed one wave of 152 x 6 resident
-    # CTAs, 560 32-row tiles fit it
+    # CTAs, 560 32-row tiles fit one of 152 x 4
     assert pick(70, 100, 100, path=0) == 1
     assert pick(40, 100, 100, path=0) == 0                   # 560 16-row tiles fit one wave
 
