@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm.so")
 FLAG_GENERIC = 0x100
 FLAG_NO_PREFETCH = 0x200
 FLAG_TEST_STALL = 0x400
+FLAG_NOALLOC = 0x800   # geometry(): the launch sdm_gx_gemm_step_noalloc would make
 FLAG_CONFIG_MASK = 0x0FF
 FLAG_CTAS_SHIFT = 12
 
@@ -24,6 +25,7 @@ STATUS = {
     -5: "SDM_GX_E_OVERLAP", -6: "SDM_GX_E_STRIDE", -7: "SDM_GX_E_GRID", -8: "SDM_GX_E_SMEM", -9: "SDM_GX_E_DEVICE",
     -10: "SDM_GX_E_PLAN", -11: "SDM_GX_E_PLAN_TI", -12: "SDM_GX_E_PLAN_DEVICE", -13: "SDM_GX_E_FLAGS",
     -14: "SDM_GX_E_CUDA", -15: "SDM_GX_E_DEVICE_FAULT", -16: "SDM_GX_E_UNSUPPORTED", -17: "SDM_GX_E_ALLOC",
+    -18: "SDM_GX_E_CAPTURE",
 }
 CODE = {v: k for k, v in STATUS.items()}
 
@@ -202,6 +204,12 @@ def geometry(d_u, x, d_dv, P: int, flags: int = 0) -> dict:
     _check(_lib.sdm_gx_gemm_geometry(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd,
                                      ctypes.byref(s), int(flags), ctypes.byref(g)), "sdm_gx_gemm_geometry")
     return g.as_dict()
+
+
+def noalloc_geometry(d_u, x, d_dv, P: int) -> dict:
+    """sdm_gx_gemm_geometry with SDM_GX_FLAG_NOALLOC: the geometry sdm_gx_gemm_step_noalloc uses for a step of this
+    shape (contiguous operands)."""
+    return geometry(d_u, x, d_dv, P, flags=FLAG_NOALLOC)
 
 
 def workspace_size(d_u, x, d_dv, P: int, flags: int = 0) -> int:

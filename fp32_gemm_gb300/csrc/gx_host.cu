@@ -230,12 +230,14 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
         return eq * tile_fma / rate(2) + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
     }
     if (ci.kind == 2) {
-        // (tile, j) units split evenly over every resident CTA (occ per SM, all busy to the end); each CTA runs up to
-        // two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one k-block
+        // (tile, j) units split evenly over every resident (virtual) CTA (occ x vctas per SM, all busy to the end);
+        // each runs up to two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one
+        // k-block
+        const int per_sm = std::max(1, occ) * std::max(1, ci.vctas);
         const double units_sm = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
-        const double units_cta = units_sm / std::max(1, occ);
+        const double units_cta = units_sm / per_sm;
         const double pieces = std::ceil(units_cta / static_cast<double>(C)) + 1.0;
-        return units_sm * ci.TI * ci.TC / rate(occ) + pieces * (1500.0 + 8.0 * C) + 2000.0;
+        return units_sm * ci.TI * ci.TC / rate(per_sm) + pieces * (1500.0 + 8.0 * C) + 2000.0;
     }
     // whole tiles: an SM runs rounds of up to `occ` concurrent CTAs; a last round with fewer CTAs runs at its own
     // (lower) rate, and each round pays a per-tile cost (pipeline fill, epilogue, the chain's dependent latency)
@@ -261,11 +263,16 @@ bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int
     return true;
 }
 
-// the stream kernel's grid for configuration k on this device: one CTA per resident slot
-int stream_ctas_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_occ[k]); }
+// The stream kernel of configuration k on this device: its launch grid (one CTA per resident slot), and the CTAs of
+// its split (each CTA hosts vctas of them, blockIdx * vctas + v).
+int stream_grid_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_occ[k]); }
+int stream_ctas_of(const DevState &d, int k) { return stream_grid_of(d, k) * std::max(1, tma_config(k).vctas); }
 
+// stream_ctas_only > 0: a stream configuration is admitted only if its split runs exactly that many CTAs (the shared
+// static workspace of sdm_gx_gemm_step_noalloc, whose per-CTA launch counters stay equal only if every launch on it
+// counts the same CTAs).
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes,
-                      int max_stream_ctas) {
+                      int stream_ctas_only) {
     if (forced >= 0) return forced;
     auto tiles_of = [&](const ConfigInfo &ci) {
         return P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
@@ -273,8 +280,8 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     auto usable = [&](int k) {
         const ConfigInfo &ci = tma_config(k);
         return d.tma_occ[k] >= 1 && config_eligible(ci, P, C, hd, stream_ctas_of(d, k), ws_bytes) &&
-               !(ci.kind == 2 && stream_ctas_of(d, k) > max_stream_ctas) && !(ci.kind == 1 && !d.slab_ok) &&
-               tiles_of(ci) < kTwo31;
+               !(ci.kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) &&
+               !(ci.kind == 1 && !d.slab_ok) && tiles_of(ci) < kTwo31;
     };
     // Small steps (no tile of 32+ outputs per thread fills the SMs): the step is bound by latency, and the measured
     // best is the configuration with the most tiles that still fit one wave (one tile per SM), i.e. the most
@@ -349,11 +356,12 @@ CUresult encode_map(CUtensorMap *m, const float *base, int64_t inner, int64_t ro
 // Build the launch description for chunks n_first .. n_first + n_count - 1 (pointers and tensor maps originate at
 // n_first). Runs after validate(); makes CUDA calls (device state, descriptor encoding).
 // ws / ws_bytes: the plan's workspace (or none). fixed_part_bytes != 0 puts the workspace's flags and launch counters
-// at that fixed offset whatever the configuration (the shared static array of sdm_gx_gemm_step_noalloc), and
-// max_stream_ctas bounds the stream kernel's grid there.
+// at that fixed offset whatever the configuration, splitting the rest of the workspace between them (the shared static
+// array of sdm_gx_gemm_step_noalloc), and stream_ctas_only (as for choose_tma_config) fixes the stream kernel's CTA
+// count there.
 int build_launch(float *du, const float *x, const float *dv, const Shape &sh, int64_t n_first, int64_t n_count,
                  unsigned flags, Launch *L, void *ws = nullptr, size_t ws_bytes = 0, size_t fixed_part_bytes = 0,
-                 int max_stream_ctas = 1 << 30) {
+                 int stream_ctas_only = 0) {
     const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
                            SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL;
     if (flags & ~known) return SDM_GX_E_FLAGS;
@@ -389,11 +397,11 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     int occ = 0;
     if (use_tma) {
         if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
-        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, max_stream_ctas);
+        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, stream_ctas_only);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
         if (!config_eligible(*ci, sh.P, sh.C, sh.hd, stream_ctas_of(d, k), ws != nullptr ? ws_bytes : 0) ||
-            (ci->kind == 2 && stream_ctas_of(d, k) > max_stream_ctas) ||
+            (ci->kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) ||
             (ci->kind == 1 && !d.slab_ok))
             return SDM_GX_E_FLAGS;
         if (ci->smem > d.optin || d.tma_occ[k] < 1) return SDM_GX_E_SMEM;
@@ -434,8 +442,9 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
             const int G = stream_ctas_of(d, k);
             const size_t need = (static_cast<size_t>(G) * ci->TI * ci->TC * 4 + 255) / 256 * 256;
             const size_t part = fixed_part_bytes ? fixed_part_bytes : need;
-            const size_t fl = (static_cast<size_t>(fixed_part_bytes ? max_stream_ctas : G) * 4 + 255) / 256 * 256;
-            if (part < need || part + 2 * fl > ws_bytes) return SDM_GX_E_FLAGS;
+            const size_t fl = fixed_part_bytes ? (ws_bytes > part ? (ws_bytes - part) / 2 / 256 * 256 : 0)
+                                               : (static_cast<size_t>(G) * 4 + 255) / 256 * 256;
+            if (part < need || static_cast<size_t>(G) * 4 > fl || part + 2 * fl > ws_bytes) return SDM_GX_E_FLAGS;
             t.part = reinterpret_cast<float *>(w);
             t.flags = reinterpret_cast<uint32_t *>(w + part);
             t.ctl = reinterpret_cast<uint32_t *>(w + part + fl);
@@ -469,7 +478,7 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     if (forced_occ > 0) occ = std::min(occ, forced_occ);
     const int64_t tiles = l.path ? l.tma.ntiles : l.gen.ntiles;
     const int64_t slots = static_cast<int64_t>(d.sms) * occ;
-    // the stream kernel runs one CTA per resident slot (its workspace is sized for that grid)
+    // the stream kernel runs one CTA per resident slot (its workspace is sized for that grid's CTAs)
     l.grid = (ci->kind == 2 && l.path == 1) ? static_cast<int>(slots)
                                              : static_cast<int>(std::max<int64_t>(1, std::min(tiles, slots)));
     sdm_gx_geom &gm = l.geom;
@@ -576,6 +585,8 @@ int sdm_gx_gemm_step_ex(float *d_u, const float *x, const float *d_dv, int64_t t
     return launch(l, ti, stream, pdl);
 }
 
+int noalloc_geometry(float *d_u, const float *x, const float *d_dv, const Shape &sh, Launch *l);
+
 int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C,
                          int64_t hd, const sdm_gx_strides *strides, unsigned flags, sdm_gx_geom *out) {
     if (out == nullptr) return SDM_GX_E_NULL;
@@ -583,6 +594,15 @@ int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, in
     int rc = ex_common(const_cast<float *>(d_u), x, d_dv, 0, N, P, C, hd, strides, &sh);
     if (rc != SDM_GX_OK) return rc;
     Launch l;
+    if (flags & SDM_GX_FLAG_NOALLOC) {
+        if (flags != SDM_GX_FLAG_NOALLOC) return SDM_GX_E_FLAGS;
+        const sdm_gx_strides c = contiguous(C, hd);
+        if (std::memcmp(&c, &sh.s, sizeof(c)) != 0) return SDM_GX_E_STRIDE;
+        rc = noalloc_geometry(const_cast<float *>(d_u), x, d_dv, sh, &l);
+        if (rc != SDM_GX_OK) return rc;
+        *out = l.geom;
+        return SDM_GX_OK;
+    }
     rc = build_launch(const_cast<float *>(d_u), x, d_dv, sh, 0, N, flags, &l);
     if (rc != SDM_GX_OK) return rc;
     *out = l.geom;
@@ -1006,10 +1026,11 @@ void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan) {
 // ---- the entry point that allocates nothing --------------------------------------------------------------------------
 // Its scratch is one static device array per device (each device's module instance has its own copy), used as the
 // stream kernel's workspace: partial sums for up to kNoAllocMaxSms CTAs of 128 x 128 tiles, then flags, then launch
-// counters. The flags and counters sit at that fixed offset whatever the tile shape, and the stream kernel's grid is
-// bounded by kNoAllocMaxSms (configurations with one CTA per SM), so that every launch on the array counts the same
-// CTAs and the per-CTA launch counters stay equal across calls of different shapes. No call allocates; every call
-// shares the array.
+// counters. The flags and counters sit at that fixed offset whatever the tile shape. Every launch on the array must
+// count the same CTAs, or the per-CTA launch counters drift apart (a hand-off would then wait for a flag that is never
+// written, or accept a stale one): build_launch is given stream_ctas_only = the SM count, which admits only stream
+// configurations that split a step over exactly one CTA per SM, and a device with more than kNoAllocMaxSms SMs is
+// refused. No call allocates; every call shares the array.
 namespace {
 constexpr int kNoAllocMaxSms = 160;
 constexpr size_t kNoAllocWords = (static_cast<size_t>(kNoAllocMaxSms) * 4 + 255) / 256 * 256;
@@ -1023,13 +1044,18 @@ struct NoAllocState {
 NoAllocState g_noalloc[kMaxDevices];
 
 // once per device, under the lock: the array's device address, and its flags and launch counters set to zero (a
-// memset of existing memory, then a device synchronisation so that every stream sees it)
-int noalloc_scratch(int dev, void **out) {
+// memset of existing memory, then a device synchronisation so that every stream sees it). That set-up cannot be part
+// of a stream capture, so a first call made while `stream` is being captured is refused.
+int noalloc_scratch(int dev, cudaStream_t stream, void **out) {
     std::lock_guard<std::mutex> lk(g_mu);
     NoAllocState &st = g_noalloc[dev];
     if (!st.init) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (cs != cudaStreamCaptureStatusNone) return SDM_GX_E_CAPTURE;
         void *a = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&a, g_sdm_gx_noalloc_scratch);
+        e = cudaGetSymbolAddress(&a, g_sdm_gx_noalloc_scratch);
         if (e != cudaSuccess) return fail_cuda(e);
         unsigned char *ctl = static_cast<unsigned char *>(a) + kNoAllocScratchBytes - 2 * kNoAllocWords;
         if ((e = cudaMemset(ctl, 0, 2 * kNoAllocWords)) != cudaSuccess || (e = cudaDeviceSynchronize()) != cudaSuccess)
@@ -1059,13 +1085,28 @@ int sdm_gx_gemm_step_noalloc(float *d_u, const float *x, const float *d_dv, int6
     // the array holds the workspace of at most kNoAllocMaxSms CTAs: a larger device is refused, not served slower
     if (dsp->sms > kNoAllocMaxSms) return SDM_GX_E_RANGE;
     void *scratch = nullptr;
-    rc = noalloc_scratch(dev, &scratch);
+    rc = noalloc_scratch(dev, stream, &scratch);
     if (rc != SDM_GX_OK) return rc;
     Launch l;
     rc = build_launch(d_u, x, d_dv, sh, ti * P, P, 0u, &l, scratch, kNoAllocScratchBytes,
-                      kNoAllocScratchBytes - 2 * kNoAllocWords, kNoAllocMaxSms);
+                      kNoAllocScratchBytes - 2 * kNoAllocWords, dsp->sms);
     if (rc != SDM_GX_OK) return rc;
     return launch(l, ti, stream, pdl);
+}
+
+// the launch sdm_gx_gemm_step_noalloc would make for a step of this shape (for sdm_gx_gemm_geometry; no set-up of
+// the array: only its address, which the geometry does not depend on)
+int noalloc_geometry(float *d_u, const float *x, const float *d_dv, const Shape &sh, Launch *l) {
+    int dev = 0;
+    const DevState *dsp = nullptr;
+    int rc = device_state(&dev, &dsp);
+    if (rc != SDM_GX_OK) return rc;
+    if (dsp->sms > kNoAllocMaxSms) return SDM_GX_E_RANGE;
+    void *a = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&a, g_sdm_gx_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return build_launch(d_u, x, d_dv, sh, 0, sh.P, 0u, l, a, kNoAllocScratchBytes,
+                        kNoAllocScratchBytes - 2 * kNoAllocWords, dsp->sms);
 }
 
 int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int64_t P, int64_t C, int64_t hd,
@@ -1151,7 +1192,7 @@ int sdm_gx_gemm_choose_config(int32_t path, int32_t sms, const int32_t *occ, int
         (path == 1 ? d.tma_occ : d.gen_occ)[k] = occ[k];
     }
     if (path == 0) return choose_generic_config(d, P, C, hd, -1);
-    const int k = choose_tma_config(d, P, C, hd, -1, ws_bytes, 1 << 30);
+    const int k = choose_tma_config(d, P, C, hd, -1, ws_bytes, 0);
     return k >= 0 ? k : SDM_GX_E_SMEM;
 }
 
@@ -1205,6 +1246,7 @@ const char *sdm_gx_strerror(int status) {
         case SDM_GX_E_DEVICE_FAULT: return "a kernel gave up a bounded wait (device error word set)";
         case SDM_GX_E_UNSUPPORTED: return "the current device is not an sm_103 GPU";
         case SDM_GX_E_ALLOC: return "host allocation failed";
+        case SDM_GX_E_CAPTURE: return "the first sdm_gx_gemm_step_noalloc call on a device sets up its static workspace and cannot run while the stream is being captured";
         default: return "unknown status";
     }
 }

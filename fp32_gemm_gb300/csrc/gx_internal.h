@@ -57,6 +57,7 @@ struct ConfigInfo {
     int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
     int kind;   // 0: tile kernel; 1: balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3);
                 // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace)
+    int vctas;  // stream kernel: virtual CTAs per CTA (the split's CTAs are blockIdx * vctas + v); 1 otherwise
 };
 
 // Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,

@@ -21,6 +21,8 @@
 //     point of coherence). d_dv is loaded into shared memory only after the wait; d_u is written only after it.
 //   * Every mbarrier wait is bounded (globaltimer); on expiry the thread sets a bit in the device error word and the
 //     CTA unwinds; the producer first waits (bounded) for the copies it issued.
+#include <utility>
+
 #include "gx_device.cuh"
 #include "gx_internal.h"
 
@@ -33,6 +35,8 @@ template <int RM_, int RN_, int WM_, int WN_, int KB_, int ST_, int MINB_, int E
 struct TCfg {
     static constexpr int EFF = EFF_;               // measured FMA-pipe efficiency at full occupancy, percent
     static constexpr int SLAB = 0;
+    static constexpr bool ROWS_OUTER = false;      // FMA order within one j: column-outer (see chain_j)
+    static constexpr bool DUPRE = false;           // stream kernel only: d_u read into registers in the last stage
     static constexpr int RM = RM_, RN = RN_;       // per-thread tile: rows x columns
     static constexpr int WM = WM_, WN = WN_;       // consumer warps along rows / columns
     static constexpr int KB = KB_, ST = ST_;       // j rows per stage, stages
@@ -87,7 +91,16 @@ __device__ __forceinline__ void chain_j(const float *__restrict__ xs, const floa
     for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
 #pragma unroll
     for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
-    if constexpr (Cfg::RM % 2 == 0) {
+    if constexpr (Cfg::RM % 2 == 0 && Cfg::ROWS_OUTER) {
+        // rows in pairs, one row pair against all of the thread's columns before the next pair: the packed x pair
+        // stays the same over RN consecutive FMAs (with 8 x 8 thread tiles the FMA pipe measured 89-90% busy inside
+        // the pipeline, against 81-82% for the column-outer order of the 8 x 4 tiles)
+#pragma unroll
+        for (int r = 0; r < Cfg::RM; r += 2) {
+#pragma unroll
+            for (int c = 0; c < Cfg::RN; ++c) dev::fma2(acc[r][c], acc[r + 1][c], a[r], a[r + 1], b[c], b[c]);
+        }
+    } else if constexpr (Cfg::RM % 2 == 0) {
         // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
 #pragma unroll
         for (int c = 0; c < Cfg::RN; ++c) {
@@ -191,6 +204,79 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
     }
 }
 
+// The staged d_u vector v (of the thread's SR * VR * SN) into registers: rows ro[sr] + er, columns co[sc] .. + VN - 1.
+template <class Cfg, int V>
+__device__ __forceinline__ void load_du_vec(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                            float (&u)[Cfg::RM][Cfg::RN]) {
+    constexpr int sr = V / (Cfg::VR * Cfg::SN), er = (V / Cfg::SN) % Cfg::VR, sc = V % Cfg::SN;
+    dev::Vec<Cfg::VN>::load(us + (ro[sr] + er) * Cfg::TC + co[sc], &u[sr * Cfg::VR + er][sc * Cfg::VN]);
+}
+
+template <class Cfg, int... V>
+__device__ __forceinline__ void load_du_rest(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                             float (&u)[Cfg::RM][Cfg::RN], std::integer_sequence<int, V...>) {
+    (load_du_vec<Cfg, Cfg::DU_PREFETCH_VECS + V>(us, ro, co, u), ...);
+}
+
+template <class Cfg, int... V>
+__device__ __forceinline__ void load_du_all(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                            float (&u)[Cfg::RM][Cfg::RN], std::integer_sequence<int, V...>) {
+    (load_du_vec<Cfg, V>(us, ro, co, u), ...);
+}
+
+// A full stage whose last NV j each also read one vector of the staged d_u tile into registers (NV = the thread's
+// d_u vectors): the epilogue that follows then needs no shared-memory reads, and the reads overlap the chain.
+template <class Cfg, int U0, int... U>
+__device__ __forceinline__ void chain_tail_du(const float *__restrict__ xs, const float *__restrict__ ds,
+                                              const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                              float (&acc)[Cfg::RM][Cfg::RN], float (&u)[Cfg::RM][Cfg::RN],
+                                              std::integer_sequence<int, U...>) {
+    ((chain_j<Cfg>(xs, ds, U0 + U, ro, co, acc), load_du_vec<Cfg, U>(us, ro, co, u)), ...);
+}
+
+template <class Cfg>
+__device__ __forceinline__ void chain_block_du(const float *__restrict__ xs, const float *__restrict__ ds,
+                                               const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                               float (&acc)[Cfg::RM][Cfg::RN], float (&u)[Cfg::RM][Cfg::RN]) {
+    constexpr int NV = Cfg::DU_PREFETCH_VECS;
+    static_assert(Cfg::KB >= NV, "a stage holds at least one j per d_u vector");
+#pragma unroll(Cfg::UNROLL)
+    for (int jj = 0; jj < Cfg::KB - NV; ++jj) chain_j<Cfg>(xs, ds, jj, ro, co, acc);
+    chain_tail_du<Cfg, Cfg::KB - NV>(xs, ds, us, ro, co, acc, u, std::make_integer_sequence<int, NV>{});
+}
+
+// The epilogue with d_u already in registers (u): d_u + acc, one rounding each, stored as in epilogue().
+template <class Cfg>
+__device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl, const float (&u)[Cfg::RM][Cfg::RN],
+                                              const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                              const float (&acc)[Cfg::RM][Cfg::RN]) {
+#pragma unroll
+    for (int sr = 0; sr < Cfg::SR; ++sr) {
+#pragma unroll
+        for (int er = 0; er < Cfg::VR; ++er) {
+            const int i = tl.i0 + ro[sr] + er;
+            if (i >= p.C) continue;
+            float *grow = p.du + static_cast<int64_t>(tl.n) * p.du_sn + static_cast<int64_t>(i) * p.du_si;
+#pragma unroll
+            for (int sc = 0; sc < Cfg::SN; ++sc) {
+                const int c = tl.c0 + co[sc];
+                if (c >= p.hd) continue;
+                float o[Cfg::VN];
+#pragma unroll
+                for (int e = 0; e < Cfg::VN; ++e)
+                    o[e] = __fadd_rn(u[sr * Cfg::VR + er][sc * Cfg::VN + e], acc[sr * Cfg::VR + er][sc * Cfg::VN + e]);
+                if (c + Cfg::VN <= p.hd) {
+                    dev::Vec<Cfg::VN>::store(grow + c, o);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < Cfg::VN; ++e)
+                        if (c + e < p.hd) grow[c + e] = o[e];
+                }
+            }
+        }
+    }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -224,11 +310,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
         int du_issued = 0;   // d_u boxes issued
         int npre = 0;        // stages of the first tile whose x box went out before the dependency wait
         bool ok = true;
+        Tile tl0{0, 0, 0};   // the first tile (decoded before the wait, so that its d_dv boxes go out right after it)
         if (t < p.ntiles) {
             dev::prefetch_tensormap(&p.tm_x);
             dev::prefetch_tensormap(&p.tm_dv);
             dev::prefetch_tensormap(&p.tm_du);
             const Tile tl = decode_tile<Cfg>(p, t);
+            tl0 = tl;
             // first what the first k-block needs (x now, d_dv into L2 for after the wait); the d_u box, needed only by
             // the epilogue, goes out last so that it does not delay the first stage
             npre = nk < Cfg::ST ? nk : Cfg::ST;
@@ -245,6 +333,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             du_issued = 1;
         }
         dev::grid_dependency_wait();
+        // the armed stages' d_dv boxes first: the first thing the consumers need after the wait
+        for (int s = 0; s < npre; ++s) {
+            if (s == 0 && p.stall_test) continue;
+            dev::tma_load_3d(base_s + Cfg::OFF_D + s * Cfg::DS_BYTES, &p.tm_dv, tl0.c0, s * Cfg::KB, tl0.n,
+                             bar0 + 8u * s);
+        }
         dev::launch_dependents();
         for (int tk = 0; t < p.ntiles && ok; t += static_cast<int>(gridDim.x), ++tk) {
             const Tile tl = decode_tile<Cfg>(p, t);
@@ -253,10 +347,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
                 const uint32_t full = bar0 + 8u * s;
                 const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
-                if (it < npre) {   // armed, x already in flight: add the d_dv box
-                    if (!(it == 0 && p.stall_test)) dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, kb * Cfg::KB, tl.n, full);
-                    continue;
-                }
+                if (it < npre) continue;   // armed before the wait, its d_dv box issued right after it
                 if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -362,6 +453,8 @@ template <int KB_, int ST_, int EFF_>
 struct SCfg {
     static constexpr int SLAB = 1;
     static constexpr int EFF = EFF_;
+    static constexpr bool ROWS_OUTER = false;
+    static constexpr bool DUPRE = false;
     static constexpr int RM = 8, RN = 4, KB = KB_, ST = ST_;
     static constexpr int WS = 4, WN = 4;           // slabs per round, warps per slab
     static constexpr int LM = 4, LN = 8;
@@ -518,6 +611,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
             du_issued = 1;
         }
         dev::grid_dependency_wait();
+        // the armed stages' d_dv boxes first: the first thing the consumers need after the wait
+        for (int q = 0; q < npre; ++q) {
+            if (q == 0 && p.stall_test) continue;
+            slab_issue<Cfg>(p, round_info(p, s_begin, s_end, q / nk), q % nk, base_s + q * Cfg::XS_BYTES,
+                            base_s + Cfg::OFF_D + q * Cfg::DS_BYTES, bar0 + 8u * q, false, true);
+        }
         dev::launch_dependents();
         for (int r = 0; r < nrounds && ok; ++r) {
             const RoundInfo R = round_info(p, s_begin, s_end, r);
@@ -527,10 +626,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
                 const uint32_t full = bar0 + 8u * s;
                 const uint32_t xs = base_s + s * Cfg::XS_BYTES;
                 const uint32_t ds = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
-                if (it < npre) {
-                    if (!(it == 0 && p.stall_test)) slab_issue<Cfg>(p, R, kb, xs, ds, full, false, true);
-                    continue;
-                }
+                if (it < npre) continue;   // armed before the wait, its d_dv boxes issued right after it
                 if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -640,18 +736,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
 // used the workspace in its own control word, which its publisher warp reads and advances right after the
 // grid-dependency wait (the next launch reads it only after this one has completed; every CTA of every launch counts,
 // so all CTAs agree on the epoch). A flag left by an earlier launch, or by an aborted one, therefore never matches.
-template <class T, int EFF_>
+template <class T, int EFF_, bool RO_ = false, int V_ = 1, bool DUPRE_ = false, int UNROLL_ = T::UNROLL>
 struct KCfg : T {
     static constexpr int SLAB = 2;
     static constexpr int EFF = EFF_;
-    static constexpr int THREADS = (T::NCW + 2) * 32;         // consumers, producer, publisher
+    static constexpr bool ROWS_OUTER = RO_;
+    static constexpr bool DUPRE = DUPRE_;   // d_u read into registers during a tile's last stage (spare registers)
+    static constexpr int DU_PREFETCH_VECS = (T::SR * T::VR * T::SN) / 2;   // of them, during the stage (register cap)
+    static constexpr int UNROLL = UNROLL_;
+    // V virtual CTAs per CTA: V independent copies of the warps and the shared-memory layout below, each running the
+    // range of one stream CTA b = blockIdx.x * V + v. They share the SM's FMA pipe, so that one copy's hand-offs and
+    // epilogues overlap the other's chains; being one CTA, they are resident together and equally old.
+    static constexpr int V = V_;
+    static constexpr int VTHREADS = (T::NCW + 2) * 32;        // one virtual CTA: consumers, producer, publisher
+    static constexpr int THREADS = V * VTHREADS;
     static constexpr int OFF_P = T::OFF_BAR;                  // the incoming partial sums [TI][TC]
     static constexpr int OFF_BAR = OFF_P + T::DU_BYTES;
     // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
     static constexpr int NBAR = 2 * T::ST + 6;
     static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
     static constexpr int OFF_PIECES = align_up(OFF_EPOCH + 4, 16);   // the CTA's Pieces (computed once)
-    static constexpr int SMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128) + 128;
+    static constexpr int VSMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128);   // one virtual CTA
+    static constexpr int SMEM = V * VSMEM + 128;
     static_assert((T::TI * T::TC * 4) % 16 == 0, "the partial-sum tile is copied in 16-byte units");
 };
 
@@ -692,8 +798,10 @@ __device__ __forceinline__ void load_frag(const float *src, int tid, float (&acc
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
+    const int vw = static_cast<int>(threadIdx.x) / Cfg::VTHREADS;   // this thread's virtual CTA
+    const int vt = static_cast<int>(threadIdx.x) % Cfg::VTHREADS;   // its thread index within it
     const uint32_t raw_s = dev::smem_addr(smem_raw);
-    const uint32_t base_s = (raw_s + 127u) & ~127u;
+    const uint32_t base_s = ((raw_s + 127u) & ~127u) + static_cast<uint32_t>(vw * Cfg::VSMEM);
     unsigned char *const base_g = smem_raw + (base_s - raw_s);
     const uint32_t bar0 = base_s + Cfg::OFF_BAR;
     const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
@@ -703,12 +811,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     const uint32_t head_stored = head_staged + 8u; // 1 arrival: the publisher's bulk store has read them
     const uint32_t epoch_known = head_stored + 8u; // 1 arrival: the publisher has put the epoch in shared memory
     volatile uint32_t *const epoch_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_EPOCH);
-    const int warp = static_cast<int>(threadIdx.x) / 32;
-    const int lane = static_cast<int>(threadIdx.x) % 32;
-    const int b = static_cast<int>(blockIdx.x);
-    const int G = static_cast<int>(gridDim.x);
+    const int warp = vt / 32;
+    const int lane = vt % 32;
+    const int b = static_cast<int>(blockIdx.x) * Cfg::V + vw;
+    const int G = static_cast<int>(gridDim.x) * Cfg::V;
 
-    if (threadIdx.x == 0) {
+    if (vt == 0) {
         for (int s = 0; s < Cfg::ST; ++s) {
             dev::mbar_init(bar0 + 8u * s, 1);
             dev::mbar_init(bar0 + 8u * (Cfg::ST + s), Cfg::NCW);
@@ -760,12 +868,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         bool part_issued = false;
         bool ok = true;
         uint32_t err_bit = kErrProducerWait;
+        const Piece P0 = piece_at(R, p.C, 0);
+        const Tile tl0 = decode_tile<Cfg>(p, P0.t);   // decoded before the wait: its d_dv boxes go out right after it
         {
             dev::prefetch_tensormap(&p.tm_x);
             dev::prefetch_tensormap(&p.tm_dv);
             dev::prefetch_tensormap(&p.tm_du);
-            const Piece P0 = piece_at(R, p.C, 0);
-            const Tile tl = decode_tile<Cfg>(p, P0.t);
+            const Tile &tl = tl0;
             const int nkb0 = (P0.j1 - P0.j0 + Cfg::KB - 1) / Cfg::KB;
             npre = nkb0 < Cfg::ST ? nkb0 : Cfg::ST;
             for (int s = 0; s < npre; ++s) {
@@ -784,6 +893,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             }
         }
         dev::grid_dependency_wait();
+        // the armed stages' d_dv boxes first: the first thing the consumers need after the wait
+        for (int s = 0; s < npre; ++s) {
+            if (s == 0 && p.stall_test) continue;
+            dev::tma_load_3d(base_s + Cfg::OFF_D + s * Cfg::DS_BYTES, &p.tm_dv, tl0.c0, P0.j0 + s * Cfg::KB, tl0.n,
+                             bar0 + 8u * s);
+        }
         dev::launch_dependents();
         for (int q = 0; q < R.count && ok; ++q) {
             const Piece P = piece_at(R, p.C, q);
@@ -812,10 +927,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
                 const uint32_t full = bar0 + 8u * s;
                 const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
                 const int j = P.j0 + kb * Cfg::KB;
-                if (it < npre) {   // armed, x already in flight: add the d_dv box
-                    if (!(it == 0 && p.stall_test)) dev::tma_load_3d(dst_d, &p.tm_dv, tl.c0, j, tl.n, full);
-                    continue;
-                }
+                if (it < npre) continue;   // armed before the wait, its d_dv box issued right after it
                 if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -874,6 +986,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     int it = 0;
     int du_used = 0;
     bool failed = false;
+    float upre[Cfg::DUPRE ? Cfg::RM : 1][Cfg::DUPRE ? Cfg::RN : 1];   // d_u of the tile being finished (DUPRE)
     for (int q = 0; q < R.count && !failed; ++q) {
         const Piece P = piece_at(R, p.C, q);
         const Tile tl = decode_tile<Cfg>(p, P.t);
@@ -883,7 +996,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
                 failed = true;
                 break;
             }
-            load_frag<Cfg>(ps, static_cast<int>(threadIdx.x), acc);
+            load_frag<Cfg>(ps, vt, acc);
         } else {
 #pragma unroll
             for (int r = 0; r < Cfg::RM; ++r) {
@@ -902,10 +1015,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
             const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
             const int nj = P.j1 - (P.j0 + kb * Cfg::KB);
-            if (nj >= Cfg::KB) {
-                chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+            if constexpr (Cfg::DUPRE) {
+                if (kb == nkb - 1 && P.kind != 1) {
+                    // the tile's last stage: its d_u (staged by then, normally long before) is read into registers
+                    // while the chain runs
+                    if (!__all_sync(0xffffffffu,
+                                    dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
+                        failed = true;
+                        break;
+                    }
+                    if (nj >= Cfg::KB) {
+                        chain_block_du<Cfg>(xs, ds, us, ro, co, acc, upre);
+                    } else {
+                        load_du_all<Cfg>(us, ro, co, upre, std::make_integer_sequence<int, Cfg::DU_PREFETCH_VECS>{});
+                        chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+                    }
+                } else if (nj >= Cfg::KB) {
+                    chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+                } else {
+                    chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+                }
             } else {
-                chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+                if (nj >= Cfg::KB) {
+                    chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
+                } else {
+                    chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
+                }
             }
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
@@ -913,17 +1048,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         if (failed) break;
         if (P.kind == 1) {
             // the head's accumulators into the (still idle) d_u buffer, visible to the publisher's bulk store
-            store_frag<Cfg>(us, static_cast<int>(threadIdx.x), acc);
+            store_frag<Cfg>(us, vt, acc);
             dev::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(head_staged);
             continue;
         }
-        if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
-            failed = true;
-            break;
+        if constexpr (Cfg::DUPRE) {
+            // the vectors not read during the last stage come from shared memory now
+            load_du_rest<Cfg>(us, ro, co, upre,
+                              std::make_integer_sequence<int, Cfg::SR * Cfg::VR * Cfg::SN - Cfg::DU_PREFETCH_VECS>{});
+            epilogue_regs<Cfg>(p, tl, upre, ro, co, acc);
+        } else {
+            if (!__all_sync(0xffffffffu,
+                            dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
+                failed = true;
+                break;
+            }
+            epilogue<Cfg>(p, tl, us, ro, co, acc);
         }
-        epilogue<Cfg>(p, tl, us, ro, co, acc);
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(du_empty);
         ++du_used;
@@ -965,9 +1108,18 @@ const void *kernel_of() {
 
 
 template <class Cfg>
+constexpr int vctas_of() {
+    if constexpr (Cfg::SLAB == 2) {
+        return Cfg::V;
+    } else {
+        return 1;
+    }
+}
+
+template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF, Cfg::SLAB};
+                      Cfg::EFF, Cfg::SLAB, vctas_of<Cfg>()};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
@@ -987,6 +1139,15 @@ using C10 = TCfg<2, 4, 1, 1, 32, 2, 8, 20>;  //   8 x  32,  1 warp
 using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 warps (rounds of four slabs)
 using C12 = KCfg<C0, 72>;                     // C0's tile with the (tile, j) work split evenly over the CTAs
 using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128 x 64 tiles, 8 warps, 2 CTAs per SM
+// The split on 128 x 128 tiles with 8 consumer warps of 8 x 8 (rows-outer FMA order, KB = 32, 3 stages, 224 KB of
+// shared memory): a third fewer shared loads per FMA (its chains run ~6% faster than C12's on the large step), half
+// of the tile's d_u read into spare registers during the tile's last stage; its epilogues cost more with 8 warps, so
+// the large step comes out even (22.3 us per step either way). The rule prefers C12; autotune measures both.
+using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, 1, true, 16>;
+// Two virtual CTAs of 128 x 64 tiles (8 consumer warps of 8 x 4 each) in one CTA per SM: like C13, but the pair is
+// resident together and equally old (two separate CTAs on one SM progress unevenly, and the later one then finishes
+// alone on 8 warps). Even with C12 on the large step (22.2 us per step).
+using C15 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 1, 70>, 70, false, 2>;
 
 struct Entry {
     ConfigInfo info;
@@ -997,7 +1158,8 @@ struct Entry {
 #define SDMGX_ENTRY(C) Entry{info_of<C>(), kernel_of<C>(), &launch_cfg<C>}
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
-                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13)};
+                          SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13),
+                          SDMGX_ENTRY(C14), SDMGX_ENTRY(C15)};
 #undef SDMGX_ENTRY
 
 }  // namespace

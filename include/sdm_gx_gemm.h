@@ -71,7 +71,8 @@ typedef enum sdm_gx_status {
     SDM_GX_E_CUDA = -14,         /* a CUDA runtime call failed: sdm_gx_last_cuda_error() has its cudaError_t     */
     SDM_GX_E_DEVICE_FAULT = -15, /* the device error word is set: a bounded wait inside a kernel gave up          */
     SDM_GX_E_UNSUPPORTED = -16,  /* the current device is not compute capability 10.3 (this build is sm_103a only) */
-    SDM_GX_E_ALLOC = -17         /* host memory for a plan could not be allocated                                */
+    SDM_GX_E_ALLOC = -17,        /* host memory for a plan could not be allocated                                */
+    SDM_GX_E_CAPTURE = -18       /* sdm_gx_gemm_step_noalloc: its first call on a device came during stream capture */
 } sdm_gx_status;
 
 /* Element strides of the three operands (innermost stride is 1 for all):
@@ -114,6 +115,9 @@ typedef struct sdm_gx_plan sdm_gx_plan;   /* opaque; host memory only */
  * every wait on that stage runs out after ~20 ms instead of the normal 2 s bound. The launch then completes, leaves d_u
  * partly unwritten, sets the device error word (read it with sdm_gx_device_error), and the context stays usable. */
 #define SDM_GX_FLAG_TEST_STALL   0x400u
+/* sdm_gx_gemm_geometry only (alone, contiguous operands): report the geometry sdm_gx_gemm_step_noalloc would use for
+ * a step of this shape. It makes no set-up of the static workspace. */
+#define SDM_GX_FLAG_NOALLOC      0x800u
 
 /*
  * One step ti on contiguous operands (the page's gx_gemm launcher, minus torch). d_u, x, d_dv are device pointers of
@@ -126,13 +130,17 @@ typedef struct sdm_gx_plan sdm_gx_plan;   /* opaque; host memory only */
 SDM_GX_API int sdm_gx_gemm_step(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t P, int64_t C, int64_t hd,
                      cudaStream_t stream, int pdl);
 
-/* One step on strided operands with the chunk count N (strides NULL: contiguous). Checks 1 <= P <= N < 2^31 and
+/* One step on strided operands with the chunk count N (strides NULL: contiguous): the page's gx_gemm launcher, whose
+ * checks (1 <= P <= N, ti < N / P, d_u disjoint from x and d_dv) it runs on whole tensors, extended to the strided
+ * views of the baddbmm call in the page's module docstring. Checks 1 <= P <= N < 2^31 and
  * 0 <= ti < N / P, the stride rules of sdm_gx_strides, and that d_u's whole [N, C, hd] span overlaps neither x's
  * nor d_dv's. flags: SDM_GX_FLAG_*. */
 SDM_GX_API int sdm_gx_gemm_step_ex(float *d_u, const float *x, const float *d_dv, int64_t ti, int64_t N, int64_t P, int64_t C,
                         int64_t hd, const sdm_gx_strides *strides, cudaStream_t stream, int pdl, unsigned flags);
 
-/* The geometry a step of this shape and layout would use on the current device (no launch). */
+/* The geometry a step of this shape and layout would use on the current device (no launch): the page's make_step
+ * records its launch geometry in step.geom and LAST_GEOM (rows per CTA, CTA cap, minimum shared memory); this reports
+ * the same facts for this library's kernels (path, tile, CTAs, one-wave check). */
 SDM_GX_API int sdm_gx_gemm_geometry(const float *d_u, const float *x, const float *d_dv, int64_t N, int64_t P, int64_t C,
                          int64_t hd, const sdm_gx_strides *strides, unsigned flags, sdm_gx_geom *out);
 
@@ -185,7 +193,8 @@ SDM_GX_API int sdm_gx_gemm_plan_create_ws(sdm_gx_plan **out, float *d_u, const f
                                           int64_t P, int64_t C, int64_t hd, const sdm_gx_strides *strides,
                                           int64_t ti_max, unsigned flags, void *workspace, size_t workspace_bytes);
 
-/* Bytes of workspace that lets a plan of this shape and layout use the stream kernel on the current device (0: no
+/* No counterpart on the pages (their kernel keeps no state between CTAs). Bytes of workspace that lets a plan of this
+ * shape and layout use the stream kernel on the current device (0: no
  * kernel of this shape uses one). About (resident CTAs) x TI x TC x 4 bytes: 9.5 MiB for 128 x 128 tiles on 152 SMs
  * (one CTA per SM), the same for 128 x 64 tiles (two per SM). */
 SDM_GX_API int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const float *d_dv, int64_t N,
@@ -216,18 +225,22 @@ SDM_GX_API int sdm_gx_gemm_autotune(float *d_u, const float *x, const float *d_d
                                     size_t workspace_bytes, int steps, cudaStream_t stream, unsigned *flags_out,
                                     int32_t *config_out, float *us_out);
 
-/* Launch step ti of a plan on `stream` (pdl as above). Errors: SDM_GX_E_PLAN (NULL / corrupt plan),
+/* Launch step ti of a plan on `stream` (pdl as above): the page's gx_gemm_plan_launch, which sets ti in the recorded
+ * launch and issues it, with its status codes -1 / -2 / -5 as the three plan errors below. Errors: SDM_GX_E_PLAN (NULL / corrupt plan),
  * SDM_GX_E_PLAN_TI (ti < 0 or ti > ti_max), SDM_GX_E_PLAN_DEVICE (current device differs), SDM_GX_E_CUDA. */
 SDM_GX_API int sdm_gx_gemm_plan_step(const sdm_gx_plan *plan, int64_t ti, cudaStream_t stream, int pdl);
 
-/* The multi-step driver: launch steps ti_begin, ti_begin +- 1, ... stopping before ti_end (descending when
+/* The multi-step driver (the page's C++ step loop bwd_steps_cuda over make_step's plan(nsteps), gx_gemm page section
+ * "the backward's C++ step loop"): launch steps ti_begin, ti_begin +- 1, ... stopping before ti_end (descending when
  * ti_begin > ti_end, e.g. (T-1, -1) for the backward's reverse loop), back to back on `stream`. With pdl != 0 every
  * launch after the first uses programmatic dependent launch, so each step's prologue overlaps its predecessor. The
  * first launch uses pdl as given too (its predecessor is whatever the caller enqueued before). Every ti in the range
  * must lie in [0, ti_max]; nothing is launched otherwise. */
 SDM_GX_API int sdm_gx_gemm_plan_run(const sdm_gx_plan *plan, int64_t ti_begin, int64_t ti_end, cudaStream_t stream, int pdl);
 
-/* The same driver with the synthetic producer in the chain: before each step ti it launches the producer, which
+/* The same driver with the synthetic producer in the chain (the page's backward runs the step's GWR kernel, which
+ * writes d_dv(ti), right before each step: module docstring, PDL paragraph; the producer stands in for it): before
+ * each step ti it launches the producer, which
  * writes d_dv chunks of step ti from S (S has d_dv's shape and strides; see sdm_gx_producer_step). Producer and step
  * launches alternate on `stream`; with pdl != 0 each is a programmatic dependent launch of the one before. The steps
  * of this driver skip the L2 prefetch of d_dv before their dependency wait (the producer is about to rewrite it). */
@@ -245,8 +258,11 @@ SDM_GX_API int sdm_gx_gemm_plan_run_producer(const sdm_gx_plan *plan, const floa
 typedef struct sdm_gx_graph sdm_gx_graph;
 SDM_GX_API int sdm_gx_gemm_plan_graph_create(sdm_gx_graph **out, const sdm_gx_plan *plan, const float *S,
                                              float *succ_out, int64_t ti_begin, int64_t ti_end, int pdl);
-/* Launch the whole captured chain on `stream` (stream-ordered, asynchronous). */
+/* Launch the whole captured chain on `stream` (stream-ordered, asynchronous), as the page's step loop issues its plan
+ * launches. Errors: SDM_GX_E_PLAN (NULL / corrupt graph), SDM_GX_E_PLAN_DEVICE, SDM_GX_E_CUDA. */
 SDM_GX_API int sdm_gx_graph_launch(const sdm_gx_graph *graph, cudaStream_t stream);
+/* Free a graph (NULL or an already destroyed handle: no effect). No counterpart on the pages: their plan is a torch
+ * tensor freed with it. */
 SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
 
 /*
@@ -261,7 +277,8 @@ SDM_GX_API void sdm_gx_graph_destroy(sdm_gx_graph *graph);
 SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *out, int64_t ti_begin, int64_t ti_end,
                                               cudaStream_t stream, int pdl);
 /*
- * The chain fed from host memory, with copies and compute overlapped: for every step ti (in the order ti_begin,
+ * No counterpart on the pages (their operands are device tensors already). The chain fed from host memory, with
+ * copies and compute overlapped: for every step ti (in the order ti_begin,
  * ti_begin +- 1, .. as sdm_gx_gemm_plan_run) the step's slices of x, d_dv and d_u are copied from the host arrays into
  * the plan's device tensors on stream `h2d`, the step runs on `compute` once they have arrived, and the step's d_u
  * slice is copied back to d_u_host on stream `d2h` once the step is done (consecutive steps are copied together in
@@ -274,7 +291,10 @@ SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *ou
 SDM_GX_API int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const float *x_host,
                                          const float *d_dv_host, int64_t ti_begin, int64_t ti_end,
                                          cudaStream_t compute, cudaStream_t h2d, cudaStream_t d2h);
+/* The geometry a plan launches every step with (the page's step.geom / LAST_GEOM for the plan's make_step). Errors:
+ * SDM_GX_E_NULL (out NULL), SDM_GX_E_PLAN (NULL / corrupt plan). Makes no CUDA call. */
 SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);
+/* Free a plan's host memory (the page's plan is a tensor freed by torch). NULL or a corrupt plan: no effect. */
 SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
 
 /*
@@ -286,17 +306,22 @@ SDM_GX_API void sdm_gx_gemm_plan_destroy(sdm_gx_plan *plan);
 SDM_GX_API int sdm_gx_producer_step(float *d_dv, const float *S, int64_t ti, int64_t P, int64_t C, int64_t hd,
                          cudaStream_t stream, int pdl);
 
-/* Registers per thread, local (spill) bytes, static shared bytes and max threads per block of a kernel:
- * path 0 = generic (config 0..2 = 16/32/64 x 64 tiles, 3 = the 128 x 64 large-tile kernel), path 1 = TMA (config
- * index as in sdm_gx_geom). out[4]. */
+/* Registers per thread, local (spill) bytes, static shared bytes and max threads per block of a kernel (the page's
+ * gx_gemm_attrs, which fills the same four int64 values for the one kernel instance it builds): path 0 = generic
+ * (config 0..2 = 16/32/64 x 64 tiles, 3 = the 128 x 64 large-tile kernel), path 1 = TMA (config index as in
+ * sdm_gx_geom). This library builds one kernel per configuration, so the call names the kernel; out[4] is as on the
+ * page. Errors: SDM_GX_E_NULL, SDM_GX_E_FLAGS (unknown path or config), SDM_GX_E_CUDA. */
 SDM_GX_API int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t out[4]);
 
-/* Static description of configuration `config` of a path (for sweeps and tests): out[0..7] = TI, TC, KB, stages,
+/* Static description of configuration `config` of a path (for sweeps and tests; the page's kernel has one tile width
+ * TC = 64 and a row count chosen per launch by _rows, this library a menu of tiles): out[0..7] = TI, TC, KB, stages,
  * threads per CTA, dynamic shared memory bytes, kind (0: tile kernel, 1: balanced slab kernel, 2: stream kernel, which
  * needs a plan workspace), consumer warps. SDM_GX_E_FLAGS for an unknown path or index. */
 SDM_GX_API int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]);
 
-/* The stream kernel's split of a step (host code shared with the kernel, for tests and tools): the step's
+/* The stream kernel's split of a step (no counterpart on the pages, which give every chunk's tile to one CTA; the
+ * chain split at a j boundary keeps the page's fixed order, module docstring formula; host code shared with the
+ * kernel, for tests and tools): the step's
  * ntiles x C units (tile t, j), ordered by (t, j), go to CTAs 0..G-1 in equal contiguous ranges (CTA b: units
  * [b W / G, (b + 1) W / G), W = ntiles x C). Needs 1 <= C <= 256 and 1 <= G <= ntiles < 2^31 (every range is then at
  * least one tile long), 0 <= b < G. With q < 0 it returns the number of pieces CTA b runs; otherwise it writes piece q
@@ -305,7 +330,8 @@ SDM_GX_API int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out
  * continuing CTA b - 1's accumulators) and returns 0. SDM_GX_E_RANGE for arguments outside those bounds. */
 SDM_GX_API int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, int32_t q, int32_t out[4]);
 
-/* The configuration a plan would choose, for a DESCRIBED device: the same rule as sdm_gx_gemm_plan_create, on the
+/* The configuration a plan would choose, for a DESCRIBED device (the counterpart of the page's _rows / one_wave rule,
+ * which also takes the SM count as an input): the same rule as sdm_gx_gemm_plan_create, on the
  * SM count `sms`, the resident CTAs per SM of every configuration of `path` (occ[k], n_occ entries =
  * sdm_gx_gemm_num_configs(path)), whether the slab kernel's 4-D x view is available (slab_ok), and a plan workspace
  * of ws_bytes (0: none). Makes no CUDA call (a diagnostic for tests and tools; a device's own values come from
@@ -315,25 +341,33 @@ SDM_GX_API int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, in
 SDM_GX_API int sdm_gx_gemm_choose_config(int32_t path, int32_t sms, const int32_t *occ, int32_t n_occ, int32_t slab_ok,
                                          int64_t P, int64_t C, int64_t hd, size_t ws_bytes);
 
-/* Number of tile configurations of a path (for sweeps and tests). */
+/* Number of tile configurations of a path (for sweeps and tests; the page's menu is its GX_GEMM rows instances). */
 SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
 
-/* The device error word of the current device: nonzero bits mean a kernel gave up a bounded wait (bit 0: a consumer
+/* The device error word of the current device. The page reports failures through its launcher's checks and the
+ * negative status codes of gx_gemm_plan_launch; its kernel has no waits that can expire, so this word has no
+ * counterpart there: it reports the bounded waits of this library's pipelined kernels. Nonzero bits mean a kernel
+ * gave up a bounded wait (bit 0: a consumer
  * waited too long for staged data, bit 1: the producer waited too long for a free stage, bit 2: a drain wait gave
  * up, bit 3: the stream kernel waited too long for another CTA's partial sums). Synchronizes the device. clear != 0
  * resets it to 0 afterwards. */
 SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
 
-/* Launches of the library's kernels since load: out[0] = step kernels, out[1] = producer kernels,
+/* Launches of the library's kernels since load (the page's PDL_LAUNCHES counters, split by kernel): out[0] = step
+ * kernels, out[1] = producer kernels,
  * out[2] = launches with programmatic dependent launch, out[3] = successor kernels. */
 SDM_GX_API void sdm_gx_launch_counts(int64_t out[4]);
 
-/* The cudaError_t of the last SDM_GX_E_CUDA returned on this host thread (0 if none). */
+/* The cudaError_t of the last SDM_GX_E_CUDA returned on this host thread, 0 if none (the page's launcher raises the
+ * CUDA error itself through C10_CUDA_CHECK; a C ABI returns SDM_GX_E_CUDA and keeps the code here). */
 SDM_GX_API int sdm_gx_last_cuda_error(void);
 
-/* A static description of a status code. */
+/* A static description of a status code: the messages of the page's launcher checks (gx_gemm's TORCH_CHECKs) and of
+ * gx_gemm_plan_launch's status codes (-1 corrupt plan, -2 step outside ti_max, -5 device mismatch), restated for
+ * sdm_gx_status. Never NULL; unknown codes give "unknown status". */
 SDM_GX_API const char *sdm_gx_strerror(int status);
 
+/* SDM_GX_ABI_VERSION of the loaded library (no counterpart on the pages: a C ABI's version check). */
 SDM_GX_API int sdm_gx_abi_version(void);
 
 #ifdef __cplusplus

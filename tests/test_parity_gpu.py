@@ -74,7 +74,7 @@ def _ragged_workload():
     return synth.Workload("ragged", 60, T=2, P=3, C=100, hd=76, x_scale="inv_sqrt_c")
 
 
-MAX_TMA_CONFIGS = 16   # the parametrisation below covers every configuration while the menu stays within this
+MAX_TMA_CONFIGS = 24   # the parametrisation below covers every configuration while the menu stays within this
 
 
 def test_config_menu_covered():

@@ -1,6 +1,7 @@
 """sdm_gx_gemm_step_noalloc (the entry point whose scratch is a static device array, so that it allocates nothing)
-against the existing stateless entry point sdm_gx_gemm_step, bit for bit, over two calls in a row: two consecutive
-steps, then the same step applied twice (each call advances the launch counters inside the shared array)."""
+against the existing stateless entry point sdm_gx_gemm_step, bit for bit, over calls in a row. The large shapes are
+checked to run the stream kernel (the only kernel that uses the array: partial sums handed between CTAs, flags, launch
+counters), and one test interleaves two shapes on the array, each result against the oracle."""
 
 import numpy as np
 import pytest
@@ -15,18 +16,30 @@ pytestmark = pytest.mark.gpu
 gx = pytest.importorskip("fp32_gemm_gb300") if torch.cuda.is_available() else None
 
 
+def _inputs(P, C, hd, seed_id=72, T=2):
+    w = synth.Workload("noalloc", seed_id, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    dev = {k: torch.from_numpy(v).cuda() for k, v in inp.items()}
+    return inp, dev
+
+
+def _uses_stream_kernel(dev, P):
+    g = gx.noalloc_geometry(dev["d_u"], dev["x"], dev["d_dv"], P)
+    return g["path"] == 1 and gx.config_info(1, g["config"])["kind"] == "stream", g
+
+
 @pytest.mark.parametrize("P,C,hd", [(200, 128, 128), (160, 100, 76), (8, 64, 64)])
 def test_noalloc_matches_existing_entry_point(P, C, hd):
-    w = synth.Workload("noalloc", 72, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
-    inp = synth.make_inputs(w)
-    x = torch.from_numpy(inp["x"]).cuda()
-    dv = torch.from_numpy(inp["d_dv"]).cuda()
-    du_ref = torch.from_numpy(inp["d_u"]).cuda()
-    du_new = du_ref.clone()
+    inp, dev = _inputs(P, C, hd)
+    stream, g = _uses_stream_kernel(dev, P)
+    if P >= 160:   # more tiles than SMs: the split over one CTA per SM, through the static array
+        assert stream and g["ctas"] == g["sms"], g
+    du_ref = dev["d_u"].clone()
+    du_new = dev["d_u"].clone()
     gx.device_error(clear=True)
     for ti in (0, 1, 1):   # two consecutive steps, then step 1 again: three calls, two in a row on each pair
-        gx.step(du_ref, x, dv, ti, P, pdl=True)
-        gx.step_noalloc(du_new, x, dv, ti, P, pdl=True)
+        gx.step(du_ref, dev["x"], dev["d_dv"], ti, P, pdl=True)
+        gx.step_noalloc(du_new, dev["x"], dev["d_dv"], ti, P, pdl=True)
     torch.cuda.synchronize()
     assert gx.device_error(clear=True) == 0
     assert_bitwise(du_new.cpu().numpy(), du_ref.cpu().numpy(), f"noalloc vs step P={P} C={C} hd={hd}")
@@ -39,8 +52,36 @@ def test_noalloc_matches_existing_entry_point(P, C, hd):
     assert np.isfinite(got).all()
 
 
+def test_noalloc_interleaved_shapes():
+    """Two shapes alternating on the one array (each call's split runs one CTA per SM, so the per-CTA launch counters
+    stay equal whatever the shape): large, ragged, large again, each step against the oracle."""
+    a_inp, a = _inputs(200, 128, 128, seed_id=73)
+    b_inp, b = _inputs(160, 100, 76, seed_id=74)
+    assert _uses_stream_kernel(a, 200)[0] and _uses_stream_kernel(b, 160)[0]
+    gx.device_error(clear=True)
+    gx.step_noalloc(a["d_u"], a["x"], a["d_dv"], 0, 200, pdl=True)
+    gx.step_noalloc(b["d_u"], b["x"], b["d_dv"], 1, 160, pdl=True)
+    gx.step_noalloc(a["d_u"], a["x"], a["d_dv"], 1, 200, pdl=True)
+    gx.step_noalloc(b["d_u"], b["x"], b["d_dv"], 0, 160, pdl=True)
+    torch.cuda.synchronize()
+    assert gx.device_error(clear=True) == 0
+    for inp, dev, P, order in ((a_inp, a, 200, [0, 1]), (b_inp, b, 160, [1, 0])):
+        want = inp["d_u"].copy()
+        oracle.run_steps(want, inp["x"], inp["d_dv"], P, order=order)
+        got = dev["d_u"].cpu().numpy()
+        for n in (0, P // 2, P - 1, P, 2 * P - 1):
+            assert_bitwise(got[n], want[n], f"interleaved P={P} chunk {n}")
+
+
 def test_noalloc_rejects_what_step_rejects():
     t = torch.zeros(4, 8, 8, device="cuda")
     with pytest.raises(gx.GxGemmError) as e:
         gx.step_noalloc(t, t, torch.zeros(4, 8, 8, device="cuda"), 0, 2)
     assert e.value.name == "SDM_GX_E_OVERLAP"
+
+
+def test_noalloc_geometry_flag_alone():
+    _, dev = _inputs(8, 64, 64)
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.geometry(dev["d_u"], dev["x"], dev["d_dv"], 8, flags=gx.FLAG_NOALLOC | gx.FLAG_GENERIC)
+    assert e.value.name == "SDM_GX_E_FLAGS"
