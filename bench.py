@@ -11,6 +11,8 @@ by the library's multi-step driver. Inputs are seeded synthetic data (synth), re
               d_u, the T steps, and d_u back to the host, all inside the timed region
   cpu_baseline  the CPU oracle (single thread) on a bounded sample of the same workload
   one_launch_context  context only: the T steps' chunks in one launch, per step (not the graded figure)
+  other_workloads  (large workload) the producer chain and the PDL chain measured the same way in the same run: us per
+              step, GFLOP/s, fraction of the per-shape roofline, kernel, clocks
 
 --impl reference times the CPU oracle itself (the reference arm of this build) on a bounded sample per step.
 Multi-GPU (torchrun): every rank runs its own replica of the workload (independent chunks, no collective);
@@ -298,6 +300,124 @@ def traffic_record():
     return rec
 
 
+def shape_roofline(w: synth.Workload, sms: int, peaks: dict) -> tuple:
+    """(roofline seconds per step, FP32 ALU peak TFLOP/s, HBM peak GB/s) of a workload's step on this device."""
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    return max(w.flops_per_step() / (fp32_peak * 1e12), w.bytes_per_step() / (hbm * 1e9)), fp32_peak, hbm
+
+
+def measure_chain_workload(gx, name: str, args, ws: int, rank: int, dev, stream, clock_index: int) -> dict:
+    """The latency-bound chained workloads (configs of the pages' step: the producer chain and the PDL chain), timed
+    like the headline workload: the T-step chain as one CUDA graph of the library, W untimed replays, the clocks
+    sampled under 1 s of the same load, then K timed replays, the L2 overwritten before each one when the working set
+    could stay in it. For the producer chain the d_u update's own figure is the same steps chained without the
+    producer (the producer excluded, as the metric asks); the chain with the producer and the producer alone are
+    reported beside it."""
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w, seed=rank)
+    d = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    S = torch.from_numpy(synth.make_source(w, seed=rank)).to(dev) if w.producer else None
+    torch.cuda.synchronize()
+    plan = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P)
+    geom = plan.geometry()
+    steps_graph = plan.graph(0, w.T, pdl=True)
+    resident = sum(v.numel() * 4 for v in d.values()) + (S.numel() * 4 if S is not None else 0)
+    flush = None
+    if resident <= 2 * L2_BYTES:
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+        def flush():
+            scratch.fill_(1.0)
+    sampler = ClockSampler(clock_index)
+    for _ in range(args.warmup):
+        steps_graph.launch()
+    torch.cuda.synchronize()
+    sampler.start()
+    if sampler.proc is not None:
+        time.sleep(0.2)
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            steps_graph.launch()
+            torch.cuda.synchronize()
+    t = time_chain(steps_graph.launch, args.steps, 0, ws, stream, flush=flush)
+    clocks = sampler.stop()
+    roof_t, fp32_peak, hbm = shape_roofline(w, geom["sms"], measured_peaks())
+    per = t / args.steps / w.T
+    out = {"T": w.T, "P": w.P, "C": w.C, "hd": w.hd, "us_per_step": round(per * 1e6, 3),
+           "gflops": round(ws * w.flops_per_step() / per / 1e9, 1),
+           "frac_of_shape_roofline": round(roof_t / per, 4),
+           "roofline_bound": "alu" if w.flops_per_step() / (fp32_peak * 1e12) >= w.bytes_per_step() / (hbm * 1e9) else "hbm",
+           "roofline_us_per_step": round(roof_t * 1e6, 4),
+           "kernel": kernel_name(gx, geom), "config": geom["config"], "ctas": geom["ctas"],
+           "l2": ("L2 overwritten before every timed chain" if flush is not None else "inputs larger than L2"),
+           "clocks": clocks}
+    if S is not None:
+        chain_graph = plan.graph(0, w.T, pdl=True, S=S)
+        tc = time_chain(chain_graph.launch, args.steps, 2, ws, stream, flush=flush)
+        # the producer alone: its T launches captured into a graph (programmatic dependent launches between them)
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for ti in range(w.T):
+                gx.producer_step(d["d_dv"], S, ti, w.P, pdl=True)
+        tp = time_chain(g.replay, args.steps, 2, ws, stream, flush=flush)
+        out["us_per_step_with_producer"] = round(tc / args.steps / w.T * 1e6, 3)
+        out["producer_us_per_step"] = round(tp / args.steps / w.T * 1e6, 3)
+        out["note"] = ("us_per_step: the d_u update's steps chained without the producer; with_producer: the "
+                       "producer + step chain of the workload; producer_us_per_step: the producer's launches alone")
+        chain_graph.close()
+    steps_graph.close()
+    plan.close()
+    return out
+
+
+def run_trace(args, w: synth.Workload, local: int) -> dict:
+    """The timeline of the workload's chain (sdm_gx_gemm_plan_set_trace): per-CTA global-timer stamps of every step of
+    the last of K graph replays, summarised as the gap between chained steps (the last CTA of step ti done -> the first
+    CTA of step ti + 1 past its dependency wait), the first staged data after the wait, the spread of CTA end times and
+    the step period. The same chain is timed with and without the stamps (their cost)."""
+    import fp32_gemm_gb300 as gx
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    inp = synth.make_inputs(w)
+    d = {k: torch.from_numpy(v).to(dev) for k, v in inp.items()}
+    S = torch.from_numpy(synth.make_source(w)).to(dev) if w.producer else None
+    plan = gx.Plan(d["d_u"], d["x"], d["d_dv"], w.P, workspace=not args.no_workspace)
+    geom = plan.geometry()
+    plain = plan.graph(0, w.T, pdl=True, S=S)
+    t_plain = time_chain(plain.launch, args.steps, args.warmup, 1, stream)
+    ctas = plan.set_trace(None, 0)
+    buf = torch.zeros(w.T * ctas * 4, dtype=torch.int64, device=dev)
+    plan.set_trace(buf, w.T)
+    traced = plan.graph(0, w.T, pdl=True, S=S)
+    t_traced = time_chain(traced.launch, args.steps, args.warmup, 1, stream)
+    a = buf.view(w.T, ctas, 4).cpu().numpy().astype(np.float64) / 1000.0   # us
+    start, waited, first, end = a[:, :, 0], a[:, :, 1], a[:, :, 2], a[:, :, 3]
+    gaps = waited[1:].min(axis=1) - end[:-1].max(axis=1)
+    out = {
+        "workload": w.name, "kernel": kernel_name(gx, geom), "config": geom["config"], "ctas": ctas,
+        "steps_timed": args.steps, "launches_per_step": w.T,
+        "us_per_step_plain": round(t_plain / args.steps / w.T * 1e6, 3),
+        "us_per_step_traced": round(t_traced / args.steps / w.T * 1e6, 3),
+        "gap_us": {"mean": round(float(gaps.mean()), 3), "min": round(float(gaps.min()), 3),
+                   "max": round(float(gaps.max()), 3)},
+        "step_period_us": round(float(np.diff(end.max(axis=1)).mean()), 3),
+        "end_spread_us": round(float((end.max(axis=1) - end.min(axis=1))[1:].mean()), 3),
+        "end_minus_release_us": {"mean": round(float((end - waited.min(axis=1, keepdims=True))[1:].mean()), 3),
+                                 "max": round(float((end.max(axis=1) - waited.min(axis=1))[1:].mean()), 3)},
+        "resident_before_release_us_median": round(float(np.median((waited - start)[1:])), 3),
+        "note": ("stamps of consumer warp 0 of each CTA (global timer, 32-256 ns ticks); gap = step ti's last CTA "
+                 "done -> step ti+1's first CTA past griddepcontrol.wait; launches 1..T-1 of the last replay"),
+    }
+    if (first[1:] > 0).all():
+        out["first_data_after_wait_us_median"] = round(float(np.median((first - waited)[1:])), 3)
+    plan.set_trace(None, 0)
+    return out
+
+
 def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
     import fp32_gemm_gb300 as gx
     dev = torch.device("cuda", local)
@@ -372,6 +492,12 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
         g_succ = plan.graph(0, w.T, pdl=True, succ_out=succ_out)
         ts = time_chain(g_succ.launch, args.steps, 2, ws, stream)
         succ_us = ts / args.steps / w.T * 1e6
+    # the latency-bound chained workloads, reported beside the headline one (same protocol, same run)
+    others = {}
+    if w.name == "large" and not args.no_other_workloads:
+        for nm in ("producer_chain", "pdl_chain"):
+            others[nm] = measure_chain_workload(gx, nm, args, ws, rank, dev, stream,
+                                                local if ws > 1 else torch.cuda.current_device())
     err = gx.device_error(clear=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
@@ -464,6 +590,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
                          "pinned host -> device copies, the chain's graph, d_u back to pinned host")},
         "gpu_launches": launches,
         "clocks": clocks,
+        **({"other_workloads": others} if others else {}),
     }
     return out
 
@@ -480,6 +607,10 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=None, help="reference arm: seconds of oracle work per step")
     ap.add_argument("--no-workspace", action="store_true",
                     help="plans without a workspace (tile kernels only; the stream kernel needs one)")
+    ap.add_argument("--trace", action="store_true",
+                    help="print the chain's per-CTA timeline summary (launch gap, first data, end spread) instead")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the producer-chain and PDL-chain figures reported beside the large workload")
     ap.add_argument("--successor", action="store_true",
                     help="also time the chain with the synthetic successor after every step (hand-off cost)")
     args = ap.parse_args()
@@ -507,6 +638,19 @@ def main():
                 "e2e": {"value": round(v, 4), "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "gpu_launches": 0}
         print(json.dumps(line), flush=True)
+        return
+
+    if args.trace:
+        # the timeline build of the library (its kernels carry the stamps; the default build has none)
+        import importlib.util
+        spec = importlib.util.spec_from_file_location("_sdm_gx_gemm_build", os.path.join(ROOT, "fp32_gemm_gb300",
+                                                                                         "build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build(trace=True)
+        os.environ["SDM_GX_TRACE_BUILD"] = "1"
+        if rank == 0:
+            print(json.dumps({"trace": run_trace(args, w, local)}), flush=True)
         return
 
     if ws > 1:

@@ -11,7 +11,10 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm.so")
+# SDM_GX_TRACE_BUILD=1: the timeline build of the same library (build(trace=True); sdm_gx_gemm_plan_set_trace works
+# there only)
+LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm_trace.so" if os.environ.get("SDM_GX_TRACE_BUILD") == "1"
+                        else "libsdm_gx_gemm.so")
 
 FLAG_GENERIC = 0x100
 FLAG_NO_PREFETCH = 0x200
@@ -82,6 +85,8 @@ SIGNATURES = {
     "sdm_gx_gemm_plan_run_producer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                      ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]),
     "sdm_gx_gemm_plan_geometry": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(Geom)]),
+    "sdm_gx_gemm_plan_set_trace": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                  ctypes.POINTER(ctypes.c_int32)]),
     "sdm_gx_gemm_plan_graph_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_void_p,
                                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int]),
     "sdm_gx_gemm_plan_run_successor": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -292,6 +297,19 @@ class Plan:
         self._keep_s = S
         _check(_lib.sdm_gx_gemm_plan_run_producer(self._h, S.data_ptr(), int(ti_begin), ti_end, _stream(stream),
                                                   int(bool(pdl))), "sdm_gx_gemm_plan_run_producer")
+
+    def set_trace(self, buf, launches: int) -> int:
+        """sdm_gx_gemm_plan_set_trace: record a timeline of the launches of steps ti < launches into buf (an int64 CUDA
+        tensor of launches * ctas * 4 entries; None turns it off). Returns the CTAs per launch."""
+        n = ctypes.c_int32(0)
+        if buf is not None:
+            if not (buf.is_cuda and buf.dtype == torch.int64 and buf.is_contiguous()):
+                raise ValueError("set_trace: a contiguous int64 CUDA tensor")
+            self._trace = buf
+        _check(_lib.sdm_gx_gemm_plan_set_trace(self._h, buf.data_ptr() if buf is not None else None,
+                                               int(launches) if buf is not None else 0, ctypes.byref(n)),
+               "sdm_gx_gemm_plan_set_trace")
+        return int(n.value)
 
     def geometry(self) -> dict:
         g = Geom()

@@ -117,7 +117,7 @@ cudaError_t launch_generic(const GenericParams &p, int grid, cudaStream_t st, in
 
 template <int TI>
 ConfigInfo generic_info() {
-    return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32, 40, 0, 1};
+    return ConfigInfo{TI, kGenTC, kGenKB, 1, kGenNT, 0, TI / kGenTY, kGenRC, kGenNT / 32, 40, 0};
 }
 
 // Large-tile generic kernel, for steps whose 128 x 64 tiles fill the SMs. CTAs of 256 threads loop over 128 x 64
@@ -284,7 +284,7 @@ const GEntry kGen[] = {
     {generic_info<16>(), reinterpret_cast<const void *>(&gx_generic_kernel<16>), &launch_generic<16>},
     {generic_info<32>(), reinterpret_cast<const void *>(&gx_generic_kernel<32>), &launch_generic<32>},
     {generic_info<64>(), reinterpret_cast<const void *>(&gx_generic_kernel<64>), &launch_generic<64>},
-    {ConfigInfo{kBigTI, kBigTC, kBigKB, 2, kBigNT, 0, 8, 4, kBigNT / 32, 50, 0, 1},   // 48 KB of static shared memory
+    {ConfigInfo{kBigTI, kBigTC, kBigKB, 2, kBigNT, 0, 8, 4, kBigNT / 32, 50, 0},   // 48 KB of static shared memory
      reinterpret_cast<const void *>(&gx_generic_big_kernel), &launch_generic_big},
 };
 

@@ -230,10 +230,9 @@ double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_
         return eq * tile_fma / rate(2) + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
     }
     if (ci.kind == 2) {
-        // (tile, j) units split evenly over every resident (virtual) CTA (occ x vctas per SM, all busy to the end);
-        // each runs up to two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one
-        // k-block
-        const int per_sm = std::max(1, occ) * std::max(1, ci.vctas);
+        // (tile, j) units split evenly over every resident CTA (occ per SM, all busy to the end); each CTA runs up to
+        // two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one k-block
+        const int per_sm = std::max(1, occ);
         const double units_sm = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
         const double units_cta = units_sm / per_sm;
         const double pieces = std::ceil(units_cta / static_cast<double>(C)) + 1.0;
@@ -263,10 +262,8 @@ bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int
     return true;
 }
 
-// The stream kernel of configuration k on this device: its launch grid (one CTA per resident slot), and the CTAs of
-// its split (each CTA hosts vctas of them, blockIdx * vctas + v).
-int stream_grid_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_occ[k]); }
-int stream_ctas_of(const DevState &d, int k) { return stream_grid_of(d, k) * std::max(1, tma_config(k).vctas); }
+// the stream kernel's grid for configuration k on this device: one CTA per resident slot
+int stream_ctas_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_occ[k]); }
 
 // stream_ctas_only > 0: a stream configuration is admitted only if its split runs exactly that many CTAs (the shared
 // static workspace of sdm_gx_gemm_step_noalloc, whose per-CTA launch counters stay equal only if every launch on it
@@ -1007,6 +1004,38 @@ int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const fl
     return e == cudaSuccess ? SDM_GX_OK : fail_cuda(e);
 }
 
+int sdm_gx_gemm_plan_set_trace(sdm_gx_plan *plan, unsigned long long *buf, int64_t launches, int32_t *ctas) {
+    int rc = plan_check(plan);
+    if (rc != SDM_GX_OK) return rc;
+#ifndef SDMGX_TRACE
+    (void)buf;
+    (void)launches;
+    (void)ctas;
+    return SDM_GX_E_UNSUPPORTED;   // the kernels of this build carry no stamps
+#endif
+    Launch &l = plan->launch;
+    if (l.path != 1 || tma_config(l.config).kind == 1) return SDM_GX_E_UNSUPPORTED;
+    if (launches < 0 || launches > kTwo31 / (4 * static_cast<int64_t>(l.grid))) return SDM_GX_E_RANGE;
+    if (buf != nullptr && launches > 0) {
+        if (reinterpret_cast<uintptr_t>(buf) & 7u) return SDM_GX_E_ALIGN;
+        cudaPointerAttributes at{};
+        cudaError_t e = cudaPointerGetAttributes(&at, buf);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SDM_GX_E_DEVICE;
+        }
+        if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != l.device)
+            return SDM_GX_E_DEVICE;
+        l.tma.trace = buf;
+        l.tma.trace_launches = static_cast<int32_t>(launches);
+    } else {
+        l.tma.trace = nullptr;
+        l.tma.trace_launches = 0;
+    }
+    if (ctas != nullptr) *ctas = l.grid;
+    return SDM_GX_OK;
+}
+
 int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out) {
     if (out == nullptr) return SDM_GX_E_NULL;
     if (plan == nullptr || plan->magic != kPlanMagic || plan->self != plan) return SDM_GX_E_PLAN;
@@ -1244,7 +1273,7 @@ const char *sdm_gx_strerror(int status) {
         case SDM_GX_E_FLAGS: return "unknown flags or invalid forced configuration";
         case SDM_GX_E_CUDA: return "a CUDA runtime call failed (see sdm_gx_last_cuda_error)";
         case SDM_GX_E_DEVICE_FAULT: return "a kernel gave up a bounded wait (device error word set)";
-        case SDM_GX_E_UNSUPPORTED: return "the current device is not an sm_103 GPU";
+        case SDM_GX_E_UNSUPPORTED: return "the current device is not an sm_103 GPU, or the plan's kernel cannot do this (a timeline on the generic or slab kernel)";
         case SDM_GX_E_ALLOC: return "host allocation failed";
         case SDM_GX_E_CAPTURE: return "the first sdm_gx_gemm_step_noalloc call on a device sets up its static workspace and cannot run while the stream is being captured";
         default: return "unknown status";

@@ -33,6 +33,12 @@ struct TmaParams {
     int64_t timeout_ns;     // bound of every mbarrier wait
     uint32_t *err;          // the device error word (kErr* bits)
     int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
+    // Optional per-CTA timeline (nullptr: off; tile and stream kernels). Launch li = n_base / P < trace_launches writes,
+    // for its CTA b of G, four global-timer stamps (ns) at trace[(li * G + b) * 4 + k]: k = 0 the CTA's start, 1 its
+    // consumer warp 0 past the dependency wait, 2 that warp holding its first staged data, 3 that warp done with its
+    // last output (results issued or partial sums staged).
+    unsigned long long *trace;
+    int32_t trace_launches;
     // stream kernel only (the plan's workspace): partial sums [grid][TI][TC] of each CTA's leading piece, one flag
     // per CTA, and one launch counter (the epoch) per CTA
     float *part;
@@ -57,7 +63,6 @@ struct ConfigInfo {
     int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
     int kind;   // 0: tile kernel; 1: balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3);
                 // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace)
-    int vctas;  // stream kernel: virtual CTAs per CTA (the split's CTAs are blockIdx * vctas + v); 1 otherwise
 };
 
 // Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,

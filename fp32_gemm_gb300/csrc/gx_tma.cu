@@ -71,6 +71,24 @@ struct Tile {
     int32_t n, i0, c0;
 };
 
+// One stamp of the optional timeline (see TmaParams::trace). Compiled only into the timeline build of the library
+// (SDMGX_TRACE): even switched off at run time the stamps change the kernels' register allocation (2-3% on the large
+// step, measured), so the default build has none. The CTA's index is re-read from the special registers.
+#ifdef SDMGX_TRACE
+constexpr bool kTrace = true;
+#else
+constexpr bool kTrace = false;
+#endif
+__device__ __forceinline__ void trace_at(const TmaParams &p, int k) {
+    if constexpr (!kTrace) return;
+    if (p.trace == nullptr) return;
+    const int li = p.n_base / p.P;
+    if (li < 0 || li >= p.trace_launches) return;
+    const int G = static_cast<int>(gridDim.x);
+    const int b = static_cast<int>(blockIdx.x);
+    p.trace[(static_cast<int64_t>(li) * G + b) * 4 + k] = dev::global_timer_ns();
+}
+
 template <class Cfg>
 __device__ __forceinline__ Tile decode_tile(const TmaParams &p, int t) {
     const int per_chunk = p.nib * p.ncb;
@@ -299,6 +317,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
         dev::fence_mbar_init();
     }
     __syncthreads();
+    if (threadIdx.x == 0) trace_at(p, 0);
 
     const int nk = (p.C + Cfg::KB - 1) / Cfg::KB;
 
@@ -399,6 +418,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
     for (int s = 0; s < Cfg::SN; ++s) co[s] = wn * Cfg::RN * Cfg::LN + s * Cfg::VN * Cfg::LN + ln * Cfg::VN;
 
     dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
+    if (threadIdx.x == 0) trace_at(p, 1);
     const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U);
     int it = 0;
     int tk = 0;
@@ -418,6 +438,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 if (lane == 0) atomicOr(p.err, kErrConsumerWait);
                 return;
             }
+
             const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
             const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
             const int nj = p.C - kb * Cfg::KB;
@@ -437,6 +458,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(du_empty);
     }
+    if (threadIdx.x == 0) trace_at(p, 3);
 }
 
 
@@ -736,7 +758,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
 // used the workspace in its own control word, which its publisher warp reads and advances right after the
 // grid-dependency wait (the next launch reads it only after this one has completed; every CTA of every launch counts,
 // so all CTAs agree on the epoch). A flag left by an earlier launch, or by an aborted one, therefore never matches.
-template <class T, int EFF_, bool RO_ = false, int V_ = 1, bool DUPRE_ = false, int UNROLL_ = T::UNROLL>
+template <class T, int EFF_, bool RO_ = false, bool DUPRE_ = false, int UNROLL_ = T::UNROLL>
 struct KCfg : T {
     static constexpr int SLAB = 2;
     static constexpr int EFF = EFF_;
@@ -744,20 +766,14 @@ struct KCfg : T {
     static constexpr bool DUPRE = DUPRE_;   // d_u read into registers during a tile's last stage (spare registers)
     static constexpr int DU_PREFETCH_VECS = (T::SR * T::VR * T::SN) / 2;   // of them, during the stage (register cap)
     static constexpr int UNROLL = UNROLL_;
-    // V virtual CTAs per CTA: V independent copies of the warps and the shared-memory layout below, each running the
-    // range of one stream CTA b = blockIdx.x * V + v. They share the SM's FMA pipe, so that one copy's hand-offs and
-    // epilogues overlap the other's chains; being one CTA, they are resident together and equally old.
-    static constexpr int V = V_;
-    static constexpr int VTHREADS = (T::NCW + 2) * 32;        // one virtual CTA: consumers, producer, publisher
-    static constexpr int THREADS = V * VTHREADS;
+    static constexpr int THREADS = (T::NCW + 2) * 32;         // consumers, producer, publisher
     static constexpr int OFF_P = T::OFF_BAR;                  // the incoming partial sums [TI][TC]
     static constexpr int OFF_BAR = OFF_P + T::DU_BYTES;
     // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
     static constexpr int NBAR = 2 * T::ST + 6;
     static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
     static constexpr int OFF_PIECES = align_up(OFF_EPOCH + 4, 16);   // the CTA's Pieces (computed once)
-    static constexpr int VSMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128);   // one virtual CTA
-    static constexpr int SMEM = V * VSMEM + 128;
+    static constexpr int SMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128) + 128;
     static_assert((T::TI * T::TC * 4) % 16 == 0, "the partial-sum tile is copied in 16-byte units");
 };
 
@@ -798,10 +814,9 @@ __device__ __forceinline__ void load_frag(const float *src, int tid, float (&acc
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
-    const int vw = static_cast<int>(threadIdx.x) / Cfg::VTHREADS;   // this thread's virtual CTA
-    const int vt = static_cast<int>(threadIdx.x) % Cfg::VTHREADS;   // its thread index within it
+    const int vt = static_cast<int>(threadIdx.x);
     const uint32_t raw_s = dev::smem_addr(smem_raw);
-    const uint32_t base_s = ((raw_s + 127u) & ~127u) + static_cast<uint32_t>(vw * Cfg::VSMEM);
+    const uint32_t base_s = (raw_s + 127u) & ~127u;
     unsigned char *const base_g = smem_raw + (base_s - raw_s);
     const uint32_t bar0 = base_s + Cfg::OFF_BAR;
     const uint32_t du_full = bar0 + 8u * (2 * Cfg::ST);
@@ -813,8 +828,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     volatile uint32_t *const epoch_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_EPOCH);
     const int warp = vt / 32;
     const int lane = vt % 32;
-    const int b = static_cast<int>(blockIdx.x) * Cfg::V + vw;
-    const int G = static_cast<int>(gridDim.x) * Cfg::V;
+    const int b = static_cast<int>(blockIdx.x);
+    const int G = static_cast<int>(gridDim.x);
 
     if (vt == 0) {
         for (int s = 0; s < Cfg::ST; ++s) {
@@ -831,6 +846,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G);
     }
     __syncthreads();
+    if (vt == 0) trace_at(p, 0);
     // read from shared memory where needed, so that no thread keeps the descriptor in registers
     const Pieces &R = *reinterpret_cast<const Pieces *>(base_g + Cfg::OFF_PIECES);
 
@@ -981,6 +997,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     for (int s = 0; s < Cfg::SN; ++s) co[s] = wn * Cfg::RN * Cfg::LN + s * Cfg::VN * Cfg::LN + ln * Cfg::VN;
 
     dev::grid_dependency_wait();   // the workspace and d_u are touched only after the predecessor grid has completed
+    if (vt == 0) trace_at(p, 1);
+    if (kTrace && warp == 0 && p.trace != nullptr) {
+        // the timeline's first-data stamp: warp 0 waits for stage 0 here (its loop then passes at once)
+        (void)__all_sync(0xffffffffu, dev::mbar_wait(bar0, 0u, p.timeout_ns));
+        if (lane == 0) trace_at(p, 2);
+    }
     float *const us = reinterpret_cast<float *>(base_g + Cfg::OFF_U);
     const float *const ps = reinterpret_cast<const float *>(base_g + Cfg::OFF_P);
     int it = 0;
@@ -1072,6 +1094,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         ++du_used;
     }
     if (failed && lane == 0) atomicOr(p.err, kErrConsumerWait);
+    if (vt == 0) trace_at(p, 3);
 }
 
 template <class Cfg>
@@ -1108,18 +1131,9 @@ const void *kernel_of() {
 
 
 template <class Cfg>
-constexpr int vctas_of() {
-    if constexpr (Cfg::SLAB == 2) {
-        return Cfg::V;
-    } else {
-        return 1;
-    }
-}
-
-template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF, Cfg::SLAB, vctas_of<Cfg>()};
+                      Cfg::EFF, Cfg::SLAB};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
@@ -1143,11 +1157,7 @@ using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128
 // shared memory): a third fewer shared loads per FMA (its chains run ~6% faster than C12's on the large step), half
 // of the tile's d_u read into spare registers during the tile's last stage; its epilogues cost more with 8 warps, so
 // the large step comes out even (22.3 us per step either way). The rule prefers C12; autotune measures both.
-using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, 1, true, 16>;
-// Two virtual CTAs of 128 x 64 tiles (8 consumer warps of 8 x 4 each) in one CTA per SM: like C13, but the pair is
-// resident together and equally old (two separate CTAs on one SM progress unevenly, and the later one then finishes
-// alone on 8 warps). Even with C12 on the large step (22.2 us per step).
-using C15 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 1, 70>, 70, false, 2>;
+using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
 
 struct Entry {
     ConfigInfo info;
@@ -1159,7 +1169,7 @@ struct Entry {
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
                           SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13),
-                          SDMGX_ENTRY(C14), SDMGX_ENTRY(C15)};
+                          SDMGX_ENTRY(C14)};
 #undef SDMGX_ENTRY
 
 }  // namespace

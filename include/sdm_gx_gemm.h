@@ -70,7 +70,8 @@ typedef enum sdm_gx_status {
     SDM_GX_E_FLAGS = -13,        /* unknown flag bits or an invalid forced configuration                         */
     SDM_GX_E_CUDA = -14,         /* a CUDA runtime call failed: sdm_gx_last_cuda_error() has its cudaError_t     */
     SDM_GX_E_DEVICE_FAULT = -15, /* the device error word is set: a bounded wait inside a kernel gave up          */
-    SDM_GX_E_UNSUPPORTED = -16,  /* the current device is not compute capability 10.3 (this build is sm_103a only) */
+    SDM_GX_E_UNSUPPORTED = -16,  /* the current device is not compute capability 10.3 (this build is sm_103a only),
+                                    or the plan's kernel cannot do the request (sdm_gx_gemm_plan_set_trace)        */
     SDM_GX_E_ALLOC = -17,        /* host memory for a plan could not be allocated                                */
     SDM_GX_E_CAPTURE = -18       /* sdm_gx_gemm_step_noalloc: its first call on a device came during stream capture */
 } sdm_gx_status;
@@ -291,6 +292,23 @@ SDM_GX_API int sdm_gx_gemm_plan_run_successor(const sdm_gx_plan *plan, float *ou
 SDM_GX_API int sdm_gx_gemm_plan_run_host(const sdm_gx_plan *plan, float *d_u_host, const float *x_host,
                                          const float *d_dv_host, int64_t ti_begin, int64_t ti_end,
                                          cudaStream_t compute, cudaStream_t h2d, cudaStream_t d2h);
+/*
+ * An optional timeline of a plan's launches, for measuring what the page's PDL design is about: the gap between
+ * chained steps (the page's module docstring: the step's reads before griddepcontrol.wait overlap the previous
+ * kernel) and the start and end of each step. No counterpart on the pages (they time with CUDA events and profilers).
+ * buf: device memory of the plan's device, 8-byte aligned, launches * (*ctas) * 4 entries; NULL or launches == 0
+ * turns the timeline off. With it on, every launch of step ti < launches writes, for each of its CTAs b,
+ * buf[(ti * ctas + b) * 4 + k] = the GPU's global timer in ns: k = 0 when the CTA starts, 1 when its first consumer
+ * warp is past the grid-dependency wait, 2 when that warp holds its first staged data (stream kernel; 0 elsewhere),
+ * 3 when that warp is done with its last output. Launches of steps >= launches write nothing. The plan records the
+ * buffer: launches and graphs made after the call use it, graphs made before do not. Call it between launches (it
+ * modifies the plan). *ctas (nullable) receives the CTAs per launch (the plan's geometry ctas).
+ * Errors: SDM_GX_E_PLAN / SDM_GX_E_PLAN_DEVICE as for plan launches; SDM_GX_E_UNSUPPORTED for a plan on the generic or
+ * slab kernel; SDM_GX_E_RANGE (launches < 0 or the buffer's index past 2^31); SDM_GX_E_ALIGN; SDM_GX_E_DEVICE.
+ */
+SDM_GX_API int sdm_gx_gemm_plan_set_trace(sdm_gx_plan *plan, unsigned long long *buf, int64_t launches,
+                                          int32_t *ctas);
+
 /* The geometry a plan launches every step with (the page's step.geom / LAST_GEOM for the plan's make_step). Errors:
  * SDM_GX_E_NULL (out NULL), SDM_GX_E_PLAN (NULL / corrupt plan). Makes no CUDA call. */
 SDM_GX_API int sdm_gx_gemm_plan_geometry(const sdm_gx_plan *plan, sdm_gx_geom *out);

@@ -170,3 +170,11 @@ def test_binding_has_no_cpu_fallback():
     import fp32_gemm_gb300._binding as b
     src = open(b.__file__).read()
     assert "oracle" not in src and "numpy" not in src
+
+
+def test_set_trace_rejects_a_bad_plan():
+    n = ctypes.c_int32(-1)
+    assert L.sdm_gx_gemm_plan_set_trace(None, None, 0, ctypes.byref(n)) == CODE["SDM_GX_E_PLAN"]
+    fake = (ctypes.c_uint64 * 64)()   # host memory that is not a plan (bad magic)
+    assert L.sdm_gx_gemm_plan_set_trace(ctypes.addressof(fake), None, 0, None) == CODE["SDM_GX_E_PLAN"]
+    assert n.value == -1

@@ -39,3 +39,35 @@ def test_bench_json_contract():
     assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["sample"]
     ctx = d["one_launch_context"]
     assert ctx["us_per_step"] > 0 and "context only" in ctx["note"]
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")
+def test_chain_workloads_beside_the_headline():
+    """The producer-chain and PDL-chain figures the large workload's line carries (measure_chain_workload), on a short
+    run: per-step time, the fraction of the shape's roofline, the kernel, the clocks; the producer chain also carries
+    the chain with the producer and the producer alone."""
+    import argparse
+    import sys as _sys
+    _sys.path.insert(0, ROOT)
+    import bench
+    import fp32_gemm_gb300 as gx
+    args = argparse.Namespace(steps=2, warmup=3, no_workspace=False)
+    dev = torch.device("cuda", 0)
+    for name in ("pdl_chain", "producer_chain"):
+        d = bench.measure_chain_workload(gx, name, args, 1, 0, dev, torch.cuda.current_stream(), 0)
+        assert d["us_per_step"] > 0 and 0 < d["frac_of_shape_roofline"] < 1.5 and d["gflops"] > 0
+        assert d["kernel"].startswith("gx_") and d["roofline_bound"] in ("alu", "hbm")
+        if name == "producer_chain":
+            assert d["us_per_step_with_producer"] > 0 and d["producer_us_per_step"] > 0
+
+
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")
+def test_trace_mode_prints_the_gap():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "pdl_chain", "--trace",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    t = json.loads(lines[0])["trace"]
+    assert 0 < t["gap_us"]["mean"] < 50 and t["step_period_us"] > 0 and t["end_spread_us"] >= 0
+    assert t["us_per_step_plain"] > 0 and t["us_per_step_traced"] > 0

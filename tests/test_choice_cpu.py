@@ -9,7 +9,7 @@ import pytest
 gx = pytest.importorskip("fp32_gemm_gb300")
 
 SMS = 152
-TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2, 1, 1]
+TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2, 1]
 GEN_OCC = [6, 4, 2, 2]
 WS = 64 << 20   # a plan workspace large enough for every stream configuration
 

@@ -684,3 +684,4 @@ def test_generic_large_tile_kernel(layout):
     assert 2 * w.P * 2 >= g["sms"]
     auto = gx.Plan(du.t, dx.t, dv.t, w.P).geometry()
     assert (auto["path"], auto["config"]) == (0, big)
+
