@@ -607,6 +607,8 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=None, help="reference arm: seconds of oracle work per step")
     ap.add_argument("--no-workspace", action="store_true",
                     help="plans without a workspace (tile kernels only; the stream kernel needs one)")
+    ap.add_argument("--chain-steps", type=int, default=None,
+                    help="a shorter chain of the same workload (T steps of the same shape): a small case for profilers")
     ap.add_argument("--trace", action="store_true",
                     help="print the chain's per-CTA timeline summary (launch gap, first data, end spread) instead")
     ap.add_argument("--no-other-workloads", action="store_true",
@@ -617,6 +619,9 @@ def main():
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_info()
     w = synth.WORKLOADS[args.workload]
+    if args.chain_steps is not None:
+        import dataclasses
+        w = dataclasses.replace(w, T=max(1, args.chain_steps))
 
     if args.impl == "reference":
         if rank != 0:

@@ -19,7 +19,9 @@ LIB_PATH = os.path.join(HERE, "lib", "libsdm_gx_gemm_trace.so" if os.environ.get
 FLAG_GENERIC = 0x100
 FLAG_NO_PREFETCH = 0x200
 FLAG_TEST_STALL = 0x400
+FLAG_TEST_NO_HANDOFF = 0x20000
 FLAG_NOALLOC = 0x800   # geometry(): the launch sdm_gx_gemm_step_noalloc would make
+FLAG_X_TRANSPOSED = 0x10000   # x stored [n][i][j] (passed here as a transpose(1, 2) view; set automatically)
 FLAG_CONFIG_MASK = 0x0FF
 FLAG_CTAS_SHIFT = 12
 
@@ -163,15 +165,27 @@ def _as3(t: torch.Tensor, rows: int, cols: int, N: int) -> torch.Tensor:
 
 
 def _operands(d_u, x, d_dv):
+    """Views, sizes and strides of the three operands. x is the logical [N, C, C] tensor x[n, j, i]; a view with unit
+    stride along j instead of i (e.g. stored.transpose(1, 2) of a [N, C(i), C(j)] tensor) is passed as stored
+    transposed (SDM_GX_FLAG_X_TRANSPOSED, returned in the last element as the flag to add)."""
     if x.dim() != 3:
         raise ValueError("gx_gemm: x is [N, C, C]")
     N, C = int(x.shape[0]), int(x.shape[1])
     hd = int(d_u.shape[-1])
-    xv = _as3(x, C, C, N)
+    xflag = 0
+    if C > 1 and x.stride(2) != 1 and x.stride(1) == 1:
+        if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+            raise TypeError("gx_gemm: operands are float32 CUDA tensors")
+        xv = x
+        xs = (x.stride(0), x.stride(2))   # chunk stride, stride between the stored rows i
+        xflag = FLAG_X_TRANSPOSED
+    else:
+        xv = _as3(x, C, C, N)
+        xs = (xv.stride(0), xv.stride(1))
     uv = _as3(d_u, C, hd, N)
     vv = _as3(d_dv, C, hd, N)
-    s = Strides(xv.stride(0), xv.stride(1), vv.stride(0), vv.stride(1), uv.stride(0), uv.stride(1))
-    return uv, xv, vv, N, C, hd, s
+    s = Strides(xs[0], xs[1], vv.stride(0), vv.stride(1), uv.stride(0), uv.stride(1))
+    return uv, xv, vv, N, C, hd, s, xflag
 
 
 def step(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, stream=None) -> None:
@@ -197,17 +211,17 @@ def step_noalloc(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, stream=None) 
 
 def step_ex(d_u, x, d_dv, ti: int, P: int, pdl: bool = False, flags: int = 0, stream=None) -> None:
     """sdm_gx_gemm_step_ex: one step on strided [N, ...] operands."""
-    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    uv, xv, vv, N, C, hd, s, xflag = _operands(d_u, x, d_dv)
     _check(_lib.sdm_gx_gemm_step_ex(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), int(ti), N, int(P), C, hd,
-                                    ctypes.byref(s), _stream(stream), int(bool(pdl)), int(flags)),
+                                    ctypes.byref(s), _stream(stream), int(bool(pdl)), int(flags) | xflag),
            "sdm_gx_gemm_step_ex")
 
 
 def geometry(d_u, x, d_dv, P: int, flags: int = 0) -> dict:
-    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    uv, xv, vv, N, C, hd, s, xflag = _operands(d_u, x, d_dv)
     g = Geom()
     _check(_lib.sdm_gx_gemm_geometry(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd,
-                                     ctypes.byref(s), int(flags), ctypes.byref(g)), "sdm_gx_gemm_geometry")
+                                     ctypes.byref(s), int(flags) | xflag, ctypes.byref(g)), "sdm_gx_gemm_geometry")
     return g.as_dict()
 
 
@@ -219,10 +233,10 @@ def noalloc_geometry(d_u, x, d_dv, P: int) -> dict:
 
 def workspace_size(d_u, x, d_dv, P: int, flags: int = 0) -> int:
     """sdm_gx_gemm_plan_workspace_size: bytes of plan workspace that let this shape use the stream kernel (0: none)."""
-    uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+    uv, xv, vv, N, C, hd, s, xflag = _operands(d_u, x, d_dv)
     n = ctypes.c_size_t(0)
     _check(_lib.sdm_gx_gemm_plan_workspace_size(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd,
-                                                ctypes.byref(s), int(flags), ctypes.byref(n)),
+                                                ctypes.byref(s), int(flags) | xflag, ctypes.byref(n)),
            "sdm_gx_gemm_plan_workspace_size")
     return int(n.value)
 
@@ -234,12 +248,12 @@ def autotune(d_u_scratch, x, d_dv, P: int, steps: int = 20, flags: int = 0, work
     is updated by the timed steps: pass a copy of d_u (same shape and strides), never d_u itself. workspace=True lets
     the stream configurations take part (a temporary allocation of the size a Plan's workspace has; the Plan must then
     have its workspace too, the default)."""
-    uv, xv, vv, N, C, hd, s = _operands(d_u_scratch, x, d_dv)
+    uv, xv, vv, N, C, hd, s, xflag = _operands(d_u_scratch, x, d_dv)
     nws = workspace_size(d_u_scratch, x, d_dv, P, flags) if workspace else 0
     ws = torch.empty(nws, dtype=torch.uint8, device=uv.device) if nws > 0 else None
     fo, co, us = ctypes.c_uint(0), ctypes.c_int32(-1), ctypes.c_float(0.0)
     _check(_lib.sdm_gx_gemm_autotune(uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N, int(P), C, hd, ctypes.byref(s),
-                                     int(flags), ws.data_ptr() if ws is not None else None, nws, int(steps),
+                                     int(flags) | xflag, ws.data_ptr() if ws is not None else None, nws, int(steps),
                                      _stream(stream), ctypes.byref(fo), ctypes.byref(co), ctypes.byref(us)),
            "sdm_gx_gemm_autotune")
     return {"flags": int(fo.value), "config": int(co.value), "us": float(us.value)}
@@ -252,7 +266,7 @@ class Plan:
     workspace=False creates it without one (sdm_gx_gemm_plan_create)."""
 
     def __init__(self, d_u, x, d_dv, P: int, ti_max: int | None = None, flags: int = 0, workspace: bool = True):
-        uv, xv, vv, N, C, hd, s = _operands(d_u, x, d_dv)
+        uv, xv, vv, N, C, hd, s, xflag = _operands(d_u, x, d_dv)
         self._keep = (d_u, x, d_dv)
         self.N, self.P, self.C, self.hd = N, int(P), C, hd
         self.T = N // int(P) if P >= 1 else 0
@@ -262,12 +276,12 @@ class Plan:
         if nws > 0:
             self._ws = torch.empty(nws, dtype=torch.uint8, device=uv.device)
             _check(_lib.sdm_gx_gemm_plan_create_ws(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
-                                                   int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags),
+                                                   int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags) | xflag,
                                                    self._ws.data_ptr(), nws), "sdm_gx_gemm_plan_create_ws")
         else:
             self._ws = None
             _check(_lib.sdm_gx_gemm_plan_create(ctypes.byref(h), uv.data_ptr(), xv.data_ptr(), vv.data_ptr(), N,
-                                                int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags)),
+                                                int(P), C, hd, ctypes.byref(s), self.ti_max, int(flags) | xflag),
                    "sdm_gx_gemm_plan_create")
         self._h = h
 

@@ -2,7 +2,8 @@
 // the synthetic producer kernel of the chained workload. sm_103a.
 //
 // Generic kernel: CTAs of 256 threads loop over tiles of TI rows x 64 columns of one chunk (grid <= resident slots);
-// a large-tile variant (below) serves steps whose 128 x 64 tiles fill the SMs.
+// a large-tile variant (below) serves steps whose 128 x 64 tiles fill the SMs. x may be given transposed (stored as
+// [n][i][j], x_si > 1): the small-tile kernel stages it with j fastest, so that its global reads stay coalesced.
 // Thread (tx, ty) of a 16 x 16 layout owns rows i0 + ty + 16 r (r < TI / 16) and columns c0 + tx + 16 q (q < 4), so
 // global reads and writes of d_u are coalesced along c. The j range is staged KB = 32 rows at a time into shared
 // memory (xs[KB][TI] from x[n, j, i], ds[KB][64] from d_dv[n, j, c], zero past C / hd) with plain loads, and every
@@ -21,7 +22,7 @@ constexpr int kGenTC = 64, kGenKB = 32, kGenNT = 256, kGenTX = 16, kGenTY = 16, 
 template <int TI>
 __global__ void __launch_bounds__(kGenNT) gx_generic_kernel(const GenericParams p) {
     constexpr int RI = TI / kGenTY;
-    __shared__ float xs[kGenKB][TI];
+    __shared__ float xs[kGenKB][TI + 1];   // + 1: the transposed staging writes columns of it without bank conflicts
     __shared__ float ds[kGenKB][kGenTC];
     const int tx = static_cast<int>(threadIdx.x) % kGenTX;
     const int ty = static_cast<int>(threadIdx.x) / kGenTX;
@@ -61,9 +62,19 @@ __global__ void __launch_bounds__(kGenNT) gx_generic_kernel(const GenericParams 
         for (int j0 = 0; j0 < p.C; j0 += kGenKB) {
             const int nj = (p.C - j0) < kGenKB ? (p.C - j0) : kGenKB;
             __syncthreads();   // the previous block's reads are done before the buffers are overwritten
-            for (int e = static_cast<int>(threadIdx.x); e < kGenKB * TI; e += kGenNT) {
-                const int jj = e / TI, ii = e - jj * TI;
-                xs[jj][ii] = (jj < nj && i0 + ii < p.C) ? xn[static_cast<int64_t>(j0 + jj) * p.x_sj + i0 + ii] : 0.0f;
+            if (p.x_si == 1) {   // x[n, j, i0 .. i0 + TI - 1] rows: i fastest
+                for (int e = static_cast<int>(threadIdx.x); e < kGenKB * TI; e += kGenNT) {
+                    const int jj = e / TI, ii = e - jj * TI;
+                    xs[jj][ii] =
+                        (jj < nj && i0 + ii < p.C) ? xn[static_cast<int64_t>(j0 + jj) * p.x_sj + i0 + ii] : 0.0f;
+                }
+            } else {             // x stored transposed: j fastest along the stored rows i
+                for (int e = static_cast<int>(threadIdx.x); e < kGenKB * TI; e += kGenNT) {
+                    const int ii = e / kGenKB, jj = e - ii * kGenKB;
+                    xs[jj][ii] = (jj < nj && i0 + ii < p.C)
+                                     ? xn[static_cast<int64_t>(i0 + ii) * p.x_si + static_cast<int64_t>(j0 + jj) * p.x_sj]
+                                     : 0.0f;
+                }
             }
             for (int e = static_cast<int>(threadIdx.x); e < kGenKB * kGenTC; e += kGenNT) {
                 const int jj = e / kGenTC, cc = e - jj * kGenTC;

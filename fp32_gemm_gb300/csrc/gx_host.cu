@@ -323,13 +323,14 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     return bk;
 }
 
-int choose_generic_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced) {
+int choose_generic_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, bool x_transposed = false) {
     if (forced >= 0) return forced;
     // a step whose 128 x 64 tiles fill the SMs runs the large-tile kernel (the last configuration); smaller steps the
-    // smallest tile that still fits one wave of resident CTAs (latency-bound)
+    // smallest tile that still fits one wave of resident CTAs (latency-bound). x given transposed: the small-tile
+    // kernels only (the large-tile kernel stages x rows with i fastest), the 64-row one for filling steps.
     const int big = generic_num_configs() - 1;
     const ConfigInfo &cg = generic_config(big);
-    if (P * ((C + cg.TI - 1) / cg.TI) * ((hd + cg.TC - 1) / cg.TC) >= d.sms) return big;
+    if (P * ((C + cg.TI - 1) / cg.TI) * ((hd + cg.TC - 1) / cg.TC) >= d.sms) return x_transposed ? big - 1 : big;
     for (int k = 0; k < big; ++k) {
         const ConfigInfo &ci = generic_config(k);
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
@@ -360,7 +361,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
                  unsigned flags, Launch *L, void *ws = nullptr, size_t ws_bytes = 0, size_t fixed_part_bytes = 0,
                  int stream_ctas_only = 0) {
     const unsigned known = SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_NO_PREFETCH | SDM_GX_FLAG_CONFIG_MASK |
-                           SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL;
+                           SDM_GX_FLAG_CTAS_MASK | SDM_GX_FLAG_TEST_STALL | SDM_GX_FLAG_X_TRANSPOSED |
+                           SDM_GX_FLAG_TEST_NO_HANDOFF;
     if (flags & ~known) return SDM_GX_E_FLAGS;
     int dev = 0;
     const DevState *dsp = nullptr;
@@ -382,7 +384,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     const sdm_gx_strides &s = sh.s;
     const int forced = static_cast<int>(flags & SDM_GX_FLAG_CONFIG_MASK) - 1;
     const int forced_occ = static_cast<int>((flags & SDM_GX_FLAG_CTAS_MASK) >> SDM_GX_FLAG_CTAS_SHIFT);
-    const bool use_tma = !(flags & SDM_GX_FLAG_GENERIC) && tma_eligible(du, x, dv, s);
+    const bool x_t = (flags & SDM_GX_FLAG_X_TRANSPOSED) != 0;   // x stored [n][i][j]: the generic kernels
+    const bool use_tma = !(flags & SDM_GX_FLAG_GENERIC) && !x_t && tma_eligible(du, x, dv, s);
     Launch l;
     l.device = dev;
     l.n_first = n_first;
@@ -434,6 +437,7 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         t.timeout_ns = (flags & SDM_GX_FLAG_TEST_STALL) ? kStallTestTimeoutNs : kWaitTimeoutNs;
         t.err = d.err;
         t.stall_test = (flags & SDM_GX_FLAG_TEST_STALL) ? 1 : 0;
+        t.handoff_test = (flags & SDM_GX_FLAG_TEST_NO_HANDOFF) ? 1 : 0;
         if (ci->kind == 2) {   // workspace: partial sums, flags, control words (sizes as stream_workspace_bytes)
             unsigned char *w = static_cast<unsigned char *>(ws);
             const int G = stream_ctas_of(d, k);
@@ -447,8 +451,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
             t.ctl = reinterpret_cast<uint32_t *>(w + part + fl);
         }
     } else {
-        if (forced >= generic_num_configs()) return SDM_GX_E_FLAGS;
-        const int k = choose_generic_config(d, sh.P, sh.C, sh.hd, forced);
+        if (forced >= generic_num_configs() || (x_t && forced == generic_num_configs() - 1)) return SDM_GX_E_FLAGS;
+        const int k = choose_generic_config(d, sh.P, sh.C, sh.hd, forced, x_t);
         ci = &generic_config(k);
         occ = std::max(1, d.gen_occ[k]);
         l.path = 0;
@@ -458,7 +462,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         g.x = x0;
         g.dv = dv0;
         g.x_sn = s.x_sn;
-        g.x_sj = s.x_sj;
+        g.x_sj = x_t ? 1 : s.x_sj;   // transposed: j is the stored rows' unit stride, x_sj their stride (along i)
+        g.x_si = x_t ? s.x_sj : 1;
         g.dv_sn = s.dv_sn;
         g.dv_sj = s.dv_sj;
         g.du_sn = s.du_sn;
@@ -618,7 +623,7 @@ int sdm_gx_gemm_plan_workspace_size(const float *d_u, const float *x, const floa
     const DevState *dsp = nullptr;
     rc = device_state(&dev, &dsp);
     if (rc != SDM_GX_OK) return rc;
-    if ((flags & SDM_GX_FLAG_GENERIC) || !tma_eligible(d_u, x, d_dv, sh.s)) return SDM_GX_OK;
+    if ((flags & (SDM_GX_FLAG_GENERIC | SDM_GX_FLAG_X_TRANSPOSED)) || !tma_eligible(d_u, x, d_dv, sh.s)) return SDM_GX_OK;
     size_t need = 0;
     for (int k = 0; k < tma_num_configs(); ++k) {
         const ConfigInfo &ci = tma_config(k);
@@ -1242,7 +1247,7 @@ int sdm_gx_device_error(uint32_t *word, int clear) {
         const uint32_t z = 0;
         if ((e = cudaMemcpyToSymbol(g_sdm_gx_error_word, &z, sizeof(z))) != cudaSuccess) return fail_cuda(e);
     }
-    return w ? SDM_GX_E_DEVICE_FAULT : SDM_GX_OK;
+    return (w & kErrFatalMask) ? SDM_GX_E_DEVICE_FAULT : SDM_GX_OK;   // a recomputed hand-off alone is no fault
 }
 
 void sdm_gx_launch_counts(int64_t out[4]) {

@@ -12,7 +12,11 @@ namespace sdmgx {
 constexpr uint32_t kErrConsumerWait = 1u;   // a consumer warp gave up waiting for a staged k-block or d_u tile
 constexpr uint32_t kErrProducerWait = 2u;   // the producer gave up waiting for a free stage / d_u buffer
 constexpr uint32_t kErrDrainWait = 4u;      // the producer gave up waiting for its own copies after an abort
-constexpr uint32_t kErrHandoffWait = 8u;    // stream kernel: the partial sums of the previous CTA did not appear
+// Informational (the results are still exact): a stream-kernel CTA's wait for the previous CTA's partial sums ran out
+// (kHandoffTimeoutNs), so it computed that tile's whole chain itself.
+constexpr uint32_t kErrHandoffRecomputed = 8u;
+constexpr uint32_t kErrFatalMask = kErrConsumerWait | kErrProducerWait | kErrDrainWait;
+constexpr int64_t kHandoffTimeoutNs = 1000000;   // 1 ms: a healthy hand-off waits microseconds
 
 // Parameters of the TMA-fed kernel. The tensor maps describe x [n][j][i], d_dv [n][j][c] and d_u [n][i][c] as 3-D
 // float32 tensors (innermost first: i / c, then rows, then chunks). Chunk coordinate of step-local chunk p:
@@ -33,6 +37,7 @@ struct TmaParams {
     int64_t timeout_ns;     // bound of every mbarrier wait
     uint32_t *err;          // the device error word (kErr* bits)
     int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
+    int32_t handoff_test;   // 1: stream kernel: publishers store but never flag their partial sums (test hook)
     // Optional per-CTA timeline (nullptr: off; tile and stream kernels). Launch li = n_base / P < trace_launches writes,
     // for its CTA b of G, four global-timer stamps (ns) at trace[(li * G + b) * 4 + k]: k = 0 the CTA's start, 1 its
     // consumer warp 0 past the dependency wait, 2 that warp holding its first staged data, 3 that warp done with its
@@ -52,6 +57,7 @@ struct GenericParams {
     const float *x;
     const float *dv;
     int64_t x_sn, x_sj, dv_sn, dv_sj, du_sn, du_si;
+    int64_t x_si;           // element stride of x along i: 1, or the stored row stride when x is given transposed
     int64_t n_base;
     int32_t P, C, hd;
     int32_t nib, ncb;

@@ -772,7 +772,8 @@ struct KCfg : T {
     // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
     static constexpr int NBAR = 2 * T::ST + 6;
     static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
-    static constexpr int OFF_PIECES = align_up(OFF_EPOCH + 4, 16);   // the CTA's Pieces (computed once)
+    static constexpr int OFF_RECOMP = OFF_EPOCH + 4;          // 1: the tail piece recomputes its tile (late hand-off)
+    static constexpr int OFF_PIECES = align_up(OFF_RECOMP + 4, 16);   // the CTA's Pieces (computed once)
     static constexpr int SMEM = align_up(OFF_PIECES + static_cast<int>(sizeof(Pieces)), 128) + 128;
     static_assert((T::TI * T::TC * 4) % 16 == 0, "the partial-sum tile is copied in 16-byte units");
 };
@@ -826,6 +827,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     const uint32_t head_stored = head_staged + 8u; // 1 arrival: the publisher's bulk store has read them
     const uint32_t epoch_known = head_stored + 8u; // 1 arrival: the publisher has put the epoch in shared memory
     volatile uint32_t *const epoch_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_EPOCH);
+    volatile uint32_t *const recomp_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_RECOMP);
     const int warp = vt / 32;
     const int lane = vt % 32;
     const int b = static_cast<int>(blockIdx.x);
@@ -865,7 +867,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
                                 Cfg::DU_TX);
                 dev::bulk_wait_all();
                 dev::fence_proxy_async_global();
-                dev::st_release_gpu(p.flags + b, epoch + 1u);
+                if (!p.handoff_test) dev::st_release_gpu(p.flags + b, epoch + 1u);
             } else {
                 atomicOr(p.err, kErrConsumerWait);
             }
@@ -883,7 +885,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         bool du0_early = false;
         bool part_issued = false;
         bool ok = true;
-        uint32_t err_bit = kErrProducerWait;
         const Piece P0 = piece_at(R, p.C, 0);
         const Tile tl0 = decode_tile<Cfg>(p, P0.t);   // decoded before the wait: its d_dv boxes go out right after it
         {
@@ -919,30 +920,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         for (int q = 0; q < R.count && ok; ++q) {
             const Piece P = piece_at(R, p.C, q);
             const Tile tl = decode_tile<Cfg>(p, P.t);
+            int j0 = P.j0;   // the piece's first j (0 for a tail that recomputes its tile)
             if (P.kind == 2) {
                 // the partial sums of CTA b - 1 (its head piece: this tile's j < ja)
                 if (!dev::mbar_wait(epoch_known, 0u, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
-                if (!dev::wait_flag(p.flags + (b - 1), *epoch_s + 1u, p.timeout_ns)) {
-                    ok = false;
-                    err_bit = kErrHandoffWait;
-                    break;
+                if (dev::wait_flag(p.flags + (b - 1), *epoch_s + 1u,
+                                   p.timeout_ns < kHandoffTimeoutNs ? p.timeout_ns : kHandoffTimeoutNs)) {
+                    *recomp_s = 0u;
+                    dev::fence_proxy_async_global();
+                    dev::mbar_arrive_expect_tx(part_full, Cfg::DU_TX);
+                    dev::bulk_load(base_s + Cfg::OFF_P, p.part + static_cast<int64_t>(b - 1) * Cfg::TI * Cfg::TC,
+                                   Cfg::DU_TX, part_full);
+                    part_issued = true;
+                } else {
+                    // CTA b - 1's partial sums are late (not resident, delayed, or withheld by the test hook): this
+                    // CTA runs the tile's whole chain itself, from j = 0 and +0, and the bits are the same. x and
+                    // d_dv are read-only, and CTA b - 1 never writes this tile's d_u. The consumers learn it from
+                    // recomp_s, ordered by the barrier's release / acquire.
+                    atomicOr(p.err, kErrHandoffRecomputed);
+                    *recomp_s = 1u;
+                    dev::mbar_arrive(part_full);
+                    j0 = 0;
                 }
-                dev::fence_proxy_async_global();
-                dev::mbar_arrive_expect_tx(part_full, Cfg::DU_TX);
-                dev::bulk_load(base_s + Cfg::OFF_P, p.part + static_cast<int64_t>(b - 1) * Cfg::TI * Cfg::TC,
-                               Cfg::DU_TX, part_full);
-                part_issued = true;
             }
-            const int nkb = (P.j1 - P.j0 + Cfg::KB - 1) / Cfg::KB;
+            const int nkb = (P.j1 - j0 + Cfg::KB - 1) / Cfg::KB;
             for (int kb = 0; kb < nkb; ++kb, ++it) {
                 const int s = it % Cfg::ST;
                 const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
                 const uint32_t full = bar0 + 8u * s;
                 const uint32_t dst_d = base_s + Cfg::OFF_D + s * Cfg::DS_BYTES;
-                const int j = P.j0 + kb * Cfg::KB;
+                const int j = j0 + kb * Cfg::KB;
                 if (it < npre) continue;   // armed before the wait, its d_dv box issued right after it
                 if (!dev::mbar_wait(bar0 + 8u * (Cfg::ST + s), ph ^ 1u, p.timeout_ns)) {
                     ok = false;
@@ -971,7 +981,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         }
         if (p.stall_test) ok = false;   // the test hook always unwinds: its consumers never took every stage
         if (!ok) {
-            atomicOr(p.err, err_bit);
+            atomicOr(p.err, kErrProducerWait);
             // Unwind as the tile kernel does: wait for the copies this thread issued before leaving.
             const int lo = it - Cfg::ST > 0 ? it - Cfg::ST : 0;
             for (int k = lo; k < it; ++k) {
@@ -1013,12 +1023,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         const Piece P = piece_at(R, p.C, q);
         const Tile tl = decode_tile<Cfg>(p, P.t);
         float acc[Cfg::RM][Cfg::RN];
+        int j0 = P.j0;
         if (P.kind == 2) {
             if (!__all_sync(0xffffffffu, dev::mbar_wait(part_full, 0u, p.timeout_ns))) {
                 failed = true;
                 break;
             }
-            load_frag<Cfg>(ps, vt, acc);
+            if (__builtin_expect(*recomp_s != 0u, 0)) {   // the hand-off was late: the whole chain here, from +0
+                j0 = 0;
+#pragma unroll
+                for (int r = 0; r < Cfg::RM; ++r) {
+#pragma unroll
+                    for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = 0.0f;
+                }
+            } else {
+                load_frag<Cfg>(ps, vt, acc);
+            }
         } else {
 #pragma unroll
             for (int r = 0; r < Cfg::RM; ++r) {
@@ -1026,7 +1046,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
                 for (int c = 0; c < Cfg::RN; ++c) acc[r][c] = 0.0f;   // +0: the chain's start value
             }
         }
-        const int nkb = (P.j1 - P.j0 + Cfg::KB - 1) / Cfg::KB;
+        const int nkb = (P.j1 - j0 + Cfg::KB - 1) / Cfg::KB;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
             const int s = it % Cfg::ST;
             const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
@@ -1036,7 +1056,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             }
             const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
             const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
-            const int nj = P.j1 - (P.j0 + kb * Cfg::KB);
+            const int nj = P.j1 - (j0 + kb * Cfg::KB);
             if constexpr (Cfg::DUPRE) {
                 if (kb == nkb - 1 && P.kind != 1) {
                     // the tile's last stage: its d_u (staged by then, normally long before) is read into registers

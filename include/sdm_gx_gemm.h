@@ -116,6 +116,15 @@ typedef struct sdm_gx_plan sdm_gx_plan;   /* opaque; host memory only */
  * every wait on that stage runs out after ~20 ms instead of the normal 2 s bound. The launch then completes, leaves d_u
  * partly unwritten, sets the device error word (read it with sdm_gx_device_error), and the context stays usable. */
 #define SDM_GX_FLAG_TEST_STALL   0x400u
+/* Test hook for a late hand-off (stream kernel): every CTA stores its head's partial sums but never flags them, so
+ * each tail's wait runs out after 1 ms and the CTA computes that tile's whole chain itself. The step's results stay
+ * exact; the device error word gets its informational bit 3. */
+#define SDM_GX_FLAG_TEST_NO_HANDOFF 0x20000u
+/* x given transposed, as the page's baddbmm call sees it (x.transpose(1, 2)): stored as [n][i][j], so that
+ * x[n, j, i] is at x + n*x_sn + i*x_sj + j (x_sj is then the stride between the stored rows i; the stride rules of
+ * sdm_gx_strides are unchanged). step_ex, geometry and plans; the generic kernels serve it (small-tile kernels, with
+ * j-fastest staging), the same chain and bits. */
+#define SDM_GX_FLAG_X_TRANSPOSED 0x10000u
 /* sdm_gx_gemm_geometry only (alone, contiguous operands): report the geometry sdm_gx_gemm_step_noalloc would use for
  * a step of this shape. It makes no set-up of the static workspace. */
 #define SDM_GX_FLAG_NOALLOC      0x800u
@@ -364,11 +373,12 @@ SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
 
 /* The device error word of the current device. The page reports failures through its launcher's checks and the
  * negative status codes of gx_gemm_plan_launch; its kernel has no waits that can expire, so this word has no
- * counterpart there: it reports the bounded waits of this library's pipelined kernels. Nonzero bits mean a kernel
- * gave up a bounded wait (bit 0: a consumer
- * waited too long for staged data, bit 1: the producer waited too long for a free stage, bit 2: a drain wait gave
- * up, bit 3: the stream kernel waited too long for another CTA's partial sums). Synchronizes the device. clear != 0
- * resets it to 0 afterwards. */
+ * counterpart there: it reports the bounded waits of this library's pipelined kernels. Bits 0-2 mean a kernel gave up
+ * a bounded wait and its step is incomplete (bit 0: a consumer waited too long for staged data, bit 1: the producer
+ * waited too long for a free stage, bit 2: a drain wait gave up); the call then returns SDM_GX_E_DEVICE_FAULT. Bit 3 is
+ * informational: a stream-kernel CTA waited more than 1 ms for the previous CTA's partial sums and computed that
+ * tile's whole chain itself, so the step's results are exact (the call returns SDM_GX_OK). Synchronizes the device.
+ * clear != 0 resets the word to 0 afterwards. */
 SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
 
 /* Launches of the library's kernels since load (the page's PDL_LAUNCHES counters, split by kernel): out[0] = step

@@ -65,3 +65,35 @@ def test_stream_kernel_expired_waits_are_reported():
     oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
     assert_bitwise(du2.host(), want, "stream kernel after the stall test")
     assert gx.device_error(clear=True) == 0
+
+
+def test_stream_kernel_late_handoff_recomputes_exactly():
+    """A hand-off that never comes (the test hook makes every CTA store but never flag its head's partial sums): each
+    tail's wait runs out after its 1 ms bound and the CTA computes that tile's whole chain itself. The steps' results
+    are still oracle-exact, the device error word carries only the informational bit 3 (device_error returns it without
+    a fault status), and a normal launch on the same workspace afterwards is exact too (the flags it finds are stale,
+    and the launch epochs tell)."""
+    k = [c for c in range(gx.num_configs(1)) if gx.config_info(1, c)["kind"] == "stream"][0]
+    w = synth.Workload("late_handoff", 78, T=2, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    du, dx, dv = (DevArray(inp[k_]) for k_ in ("d_u", "x", "d_dv"))
+    gx.device_error(clear=True)
+    late = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.FLAG_TEST_NO_HANDOFF | gx.config_flag(k))
+    assert late.geometry()["config"] == k
+    late.run(pdl=True)
+    torch.cuda.synchronize()
+    word = gx.device_error(clear=True)
+    assert word == 8, f"expected only the informational hand-off bit: {word:#x}"
+    want = inp["d_u"].copy()
+    oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
+    assert_bitwise(du.host(), want, "late hand-off, recomputed")
+    assert du.guards_intact()
+    rc = gx.lib().sdm_gx_device_error(__import__("ctypes").byref(__import__("ctypes").c_uint32(0)), 1)
+    assert rc == 0
+    # the same buffers again with a normal plan of the same configuration
+    ok = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+    ok.run(pdl=True)
+    torch.cuda.synchronize()
+    oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
+    assert_bitwise(du.host(), want, "normal launch after the late hand-offs")
+    assert gx.device_error(clear=True) == 0

@@ -293,30 +293,106 @@ def test_large_full_size_bench_configuration_sampled():
     assert_bitwise(got[n, i, c], pts, "large sampled outputs")
 
 
+def _cross_pattern(P, C, hd, pattern, seed):
+    """One step's operands in one of the six value patterns of the gx_gemm page's qualification probe (its
+    `_probe_inputs`: normal values with signed zeros, half zeros, magnitudes spread over 2^-60..2^60 with values near
+    the float32 maximum, denormal-scale products, rows that nearly cancel, and sprinkled NaN / infinities / -0 /
+    subnormals / near-maximum values). Our own generator (numpy, seeded); x [P, C, C], d_dv and d_u [P, C, hd]."""
+    g = np.random.default_rng(seed)
+    x = (g.standard_normal((P, C, C)) * 0.25).astype(np.float32)
+    dv = g.standard_normal((P, C, hd)).astype(np.float32)
+    du = g.standard_normal((P, C, hd)).astype(np.float32)
+    if pattern == "normal":
+        x.reshape(-1)[::7] = -0.0
+        dv.reshape(-1)[::11] = 0.0
+        du.reshape(-1)[::13] = -0.0
+    elif pattern == "zeros":
+        x[g.random(x.shape) < 0.5] = -0.0
+        dv[g.random(dv.shape) < 0.5] = 0.0
+        du[g.random(du.shape) < 0.5] = -0.0
+    elif pattern == "large":
+        for t in (x, dv, du):
+            t *= np.exp2(g.integers(-60, 61, t.shape)).astype(np.float32)
+        x.reshape(-1)[::17] = 3.0e38
+        dv.reshape(-1)[::19] = -3.0e38
+    elif pattern == "denormal":
+        x *= np.float32(1e-20)
+        dv *= np.float32(1e-19)
+        du *= np.float32(1e-38)
+        du.reshape(-1)[::5] = np.float32(1e-41)
+    elif pattern == "cancel":
+        x = (np.sign(g.standard_normal((P, C, C))) * (1.0 + g.random((P, C, C)))).astype(np.float32)
+        dv *= np.float32(1e4)
+        h = C // 2
+        dv[:, 1:2 * h:2, :] = (-dv[:, 0:2 * h:2, :] * (1.0 + 1e-3 * g.standard_normal((P, h, hd)))).astype(np.float32)
+        du *= np.float32(1e-3)
+    elif pattern == "special":
+        vals = np.array([np.nan, np.inf, -np.inf, -0.0, 1e-41, 3.4e38, -3.4e38], np.float32)
+        for t, k in ((dv, 64), (x, 16), (du, 32)):
+            fl = t.reshape(-1)
+            pos = g.permutation(fl.size)[:k]
+            fl[pos] = vals[np.arange(k) % vals.size]
+    return x, dv, du
+
+
+def _forced_nan(x, dv, du):
+    """Outputs that IEEE arithmetic makes NaN in ANY summation order: a NaN operand in the output's chain or its d_u,
+    a zero times an infinity, or exact infinite products (or d_u) of both signs. (Infinities reached by overflow are
+    order-dependent and left out.)"""
+    x64, v64, u64 = x.astype(np.float64), dv.astype(np.float64), du.astype(np.float64)
+    with np.errstate(invalid="ignore", over="ignore"):
+        prod = x64[:, :, :, None] * v64[:, :, None, :]          # [P, j, i, c]
+    nan = np.isnan(prod).any(axis=1) | np.isnan(u64)
+    xinf, vinf = np.isinf(x64), np.isinf(v64)
+    pos = ((xinf[:, :, :, None] | vinf[:, :, None, :]) & (prod > 0)).any(axis=1) | (np.isposinf(u64))
+    neg = ((xinf[:, :, :, None] | vinf[:, :, None, :]) & (prod < 0)).any(axis=1) | (np.isneginf(u64))
+    return nan | (pos & neg)
+
+
 def test_informative_cublas_cross_check():
-    """The pages' second reference: cuBLAS FP32 batched GEMM (torch.baddbmm, TF32 off) computed the same chain on the
-    configurations the page tested, but that is not a cuBLAS guarantee. Informative: report the bitwise agreement;
-    require only that both lie within the recursive-summation error bound of each other."""
-    w = synth.WORKLOADS["pdl_chain"]
-    inp = synth.make_inputs(w, N=w.P)
-    x = torch.from_numpy(inp["x"]).cuda()
-    dv = torch.from_numpy(inp["d_dv"]).cuda()
-    du = torch.from_numpy(inp["d_u"]).cuda()
-    ours = du.clone()
-    gx.Plan(ours, x, dv, w.P).step(0)
+    """The pages' second reference: cuBLAS FP32 batched GEMM (torch.baddbmm on the x.transpose(1, 2) view, TF32 off)
+    computed the same chain on the configurations the page tested, but that is not a cuBLAS guarantee. Informative,
+    as the page's qualification probe is set up: the six value patterns against every 4-byte base offset mod 256 of
+    each operand (the others 256-byte aligned; 16-byte-aligned offsets take the TMA kernels, the others the generic
+    one), and the bitwise agreement printed per pattern and operand. Required: finite results of both within the
+    recursive-summation error bound of each other, and NaN from both wherever IEEE forces it in every order."""
+    P, C, hd = 3, 64, 96
+    bound_k = 2 * (C + 1) * 2.0 ** -24
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
+    rows = []
     try:
-        ref = torch.baddbmm(du, x.transpose(1, 2), dv)
+        for pi, pattern in enumerate(("normal", "zeros", "large", "denormal", "cancel", "special")):
+            x, dv, du = _cross_pattern(P, C, hd, pattern, 20261203 + 7919 * pi)
+            with np.errstate(invalid="ignore", over="ignore"):
+                scale = np.abs(du).astype(np.float64) + np.einsum("nji,njc->nic", np.abs(x).astype(np.float64),
+                                                                   np.abs(dv).astype(np.float64))
+            forced = _forced_nan(x, dv, du)
+            for operand in ("d_u", "x", "d_dv"):
+                agree = []
+                for res in range(0, 256, 4):
+                    off = {"d_u": 0, "x": 0, "d_dv": 0}
+                    off[operand] = res // 4
+                    u_d = DevArray(du, offset_floats=off["d_u"])
+                    x_d = DevArray(x, offset_floats=off["x"])
+                    v_d = DevArray(dv, offset_floats=off["d_dv"])
+                    ref = torch.baddbmm(u_d.t, x_d.t.transpose(1, 2), v_d.t)
+                    gx.step_ex(u_d.t, x_d.t, v_d.t, 0, P)
+                    torch.cuda.synchronize()
+                    a, b = u_d.host(), ref.cpu().numpy()
+                    assert u_d.guards_intact()
+                    agree.append(float(np.mean(a.view(np.uint32) == b.view(np.uint32))))
+                    both = np.isfinite(a) & np.isfinite(b)
+                    with np.errstate(invalid="ignore"):
+                        err = np.abs(a.astype(np.float64) - b.astype(np.float64))
+                    assert np.all(err[both] <= bound_k * scale[both] * 1.0001 + 1e-44), (pattern, operand, res)
+                    assert np.isnan(a[forced]).all() and np.isnan(b[forced]).all(), (pattern, operand, res)
+                rows.append((pattern, operand, min(agree), float(np.mean(agree)), max(agree)))
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
-    torch.cuda.synchronize()
-    a, b = ours.cpu().numpy(), ref.cpu().numpy()
-    same = float(np.mean(a.view(np.uint32) == b.view(np.uint32)))
-    print(f"bitwise agreement with cuBLAS baddbmm: {same:.4f}")
-    bound = 2 * (w.C + 1) * 2.0 ** -24 * (np.abs(inp["d_u"]) + np.einsum("nji,njc->nic", np.abs(inp["x"]),
-                                                                           np.abs(inp["d_dv"])))
-    assert np.all(np.abs(a.astype(np.float64) - b) <= bound * 1.0001 + 1e-30)
+    print("\nbitwise agreement with cuBLAS baddbmm over 64 base offsets mod 256 (min / mean / max):")
+    for pattern, operand, lo, mean, hi in rows:
+        print(f"  {pattern:8s} offset on {operand:5s}: {lo:.4f} / {mean:.4f} / {hi:.4f}")
 
 
 @pytest.mark.parametrize("graph", [False, True])
@@ -685,3 +761,53 @@ def test_generic_large_tile_kernel(layout):
     auto = gx.Plan(du.t, dx.t, dv.t, w.P).geometry()
     assert (auto["path"], auto["config"]) == (0, big)
 
+
+
+@pytest.mark.parametrize("vset", synth.VALUE_SETS)
+def test_transposed_x_view_edge(vset):
+    """x given as the page's baddbmm call sees it: stored as [n][i][j] (x.transpose(1, 2) of the stored tensor is the
+    logical x[n, j, i]). The edge workload's ragged shape (C = 48, hd = 99), every value set, a PDL chain of its T
+    steps; bit-exact against the oracle on the logical x, guards and x untouched."""
+    w = synth.WORKLOADS["edge"]
+    inp = synth.make_inputs(w, value_set=vset, hd=99)
+    want, _ = _oracle_steps(inp, w.P, range(w.T))
+    stored = np.ascontiguousarray(inp["x"].transpose(0, 2, 1))   # [n][i][j]
+    dxs = DevArray(stored)
+    du, dv = DevArray(inp["d_u"]), DevArray(inp["d_dv"])
+    xview = dxs.t.transpose(1, 2)
+    pl = gx.Plan(du.t, xview, dv.t, w.P)
+    g = pl.geometry()
+    assert g["path"] == 0 and g["config"] < gx.num_configs(0) - 1, g
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"transposed x {vset}")
+    assert du.guards_intact() and dxs.guards_intact() and dv.guards_intact()
+    assert np.array_equal(dxs.host().view(np.uint32), stored.view(np.uint32))
+
+
+@pytest.mark.parametrize("P,C,hd", [(160, 100, 76), (200, 128, 128), (3, 256, 40)])
+def test_transposed_x_view_shapes(P, C, hd):
+    """The transposed x on filling steps (the 64-row generic kernel), the large step's chunk shape, and C = 256 with a
+    narrow hd; through step_ex (one step), a plan graph replayed twice in reverse, and against the row-major x."""
+    T = 2
+    w = synth.Workload("xt", 77, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, [1, 0] * 2)
+    stored = np.ascontiguousarray(inp["x"].transpose(0, 2, 1))
+    xs = torch.from_numpy(stored).cuda()
+    du = torch.from_numpy(inp["d_u"]).cuda()
+    dv = torch.from_numpy(inp["d_dv"]).cuda()
+    pl = gx.Plan(du, xs.transpose(1, 2), dv, P)
+    assert pl.geometry()["path"] == 0
+    gr = pl.graph(T - 1, -1, pdl=True)
+    gr.launch()
+    gr.launch()
+    torch.cuda.synchronize()
+    assert_bitwise(du.cpu().numpy(), want, f"transposed x P={P} C={C} hd={hd}")
+    # one step through step_ex equals the same step on the row-major x
+    du1 = torch.from_numpy(inp["d_u"]).cuda()
+    du2 = du1.clone()
+    gx.step_ex(du1, xs.transpose(1, 2), dv, 1, P, pdl=False)
+    gx.step_ex(du2, torch.from_numpy(inp["x"]).cuda(), dv, 1, P, pdl=False)
+    torch.cuda.synchronize()
+    assert_bitwise(du1.cpu().numpy(), du2.cpu().numpy(), "transposed vs row-major x")
