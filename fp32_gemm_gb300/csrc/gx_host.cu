@@ -446,6 +446,7 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
             const size_t fl = fixed_part_bytes ? (ws_bytes > part ? (ws_bytes - part) / 2 / 256 * 256 : 0)
                                                : (static_cast<size_t>(G) * 4 + 255) / 256 * 256;
             if (part < need || static_cast<size_t>(G) * 4 > fl || part + 2 * fl > ws_bytes) return SDM_GX_E_FLAGS;
+            t.stream_kappa = stream_kappa(t.ntiles, t.C, G);
             t.part = reinterpret_cast<float *>(w);
             t.flags = reinterpret_cast<uint32_t *>(w + part);
             t.ctl = reinterpret_cast<uint32_t *>(w + part + fl);
@@ -1200,7 +1201,7 @@ int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]) {
 int sdm_gx_gemm_stream_piece(int64_t ntiles, int32_t C, int32_t G, int32_t b, int32_t q, int32_t out[4]) {
     if (out == nullptr) return SDM_GX_E_NULL;
     if (C < 1 || C > 256 || G < 1 || ntiles < G || ntiles >= kTwo31 || b < 0 || b >= G) return SDM_GX_E_RANGE;
-    const Pieces R = cta_pieces(static_cast<int>(ntiles), C, b, G);
+    const Pieces R = cta_pieces(static_cast<int>(ntiles), C, b, G, stream_kappa(ntiles, C, G));
     if (q < 0) return R.count;
     if (q >= R.count) return SDM_GX_E_RANGE;
     const Piece pc = piece_at(R, C, q);

@@ -38,6 +38,7 @@ struct TmaParams {
     uint32_t *err;          // the device error word (kErr* bits)
     int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
     int32_t handoff_test;   // 1: stream kernel: publishers store but never flag their partial sums (test hook)
+    int32_t stream_kappa;   // stream kernel: the split's charge per tile boundary in a CTA's range (stream_kappa())
     // Optional per-CTA timeline (nullptr: off; tile and stream kernels). Launch li = n_base / P < trace_launches writes,
     // for its CTA b of G, four global-timer stamps (ns) at trace[(li * G + b) * 4 + k]: k = 0 the CTA's start, 1 its
     // consumer warp 0 past the dependency wait, 2 that warp holding its first staged data, 3 that warp done with its
@@ -94,10 +95,21 @@ struct Pieces {
     int has_head, has_tail, first_full, nfull, count;
 };
 
-__host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G) {
-    const int64_t W = static_cast<int64_t>(ntiles) * C;
-    const int64_t lo = static_cast<int64_t>(b) * W / G;
-    const int64_t hi = static_cast<int64_t>(b + 1) * W / G;
+// unit u of the step at cost u + kappa * floor(u / C) (every tile begun after the first costs kappa units more) back
+// from a cost y: inside tile t the cost runs t (C + kappa) .. t (C + kappa) + C; the kappa after it maps to the
+// tile's end
+__host__ __device__ inline int64_t unit_at_cost(int64_t y, int C, int kappa) {
+    const int64_t t = y / (C + kappa);
+    const int64_t r = y - t * (C + kappa);
+    return t * C + (r < C ? r : C);
+}
+
+__host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G, int kappa = 0) {
+    // CTA b takes the units between costs b F / G and (b + 1) F / G, F = the step's total cost: with kappa = 0 equal
+    // ranges of units; with kappa > 0 a range that holds a tile boundary (one more piece) holds kappa fewer units
+    const int64_t F = static_cast<int64_t>(ntiles) * (C + kappa) - kappa;   // no charge after the last tile
+    const int64_t lo = unit_at_cost(static_cast<int64_t>(b) * F / G, C, kappa);
+    const int64_t hi = unit_at_cost(static_cast<int64_t>(b + 1) * F / G, C, kappa);
     Pieces R;
     R.ta = static_cast<int>(lo / C);
     R.ja = static_cast<int>(lo - static_cast<int64_t>(R.ta) * C);
@@ -110,6 +122,17 @@ __host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G) {
     R.nfull = last_full >= R.first_full ? last_full - R.first_full + 1 : 0;
     R.count = R.has_head + R.nfull + R.has_tail;
     return R;
+}
+
+// The split's charge per tile boundary (units of (tile, j)): a CTA whose range holds one more boundary runs one more
+// piece (a publication or a reload of partial sums and an epilogue, ~1 us of stalled consumers on the large step), so
+// it takes fewer units. Only when every range then stays longer than one tile (W / G >= C + 2 kappa).
+#ifndef SDMGX_STREAM_KAPPA
+#define SDMGX_STREAM_KAPPA 12
+#endif
+constexpr int kStreamKappa = SDMGX_STREAM_KAPPA;
+inline int stream_kappa(int64_t ntiles, int C, int G) {
+    return static_cast<int64_t>(ntiles) * C / G >= C + 2 * kStreamKappa ? kStreamKappa : 0;
 }
 
 // piece q of a CTA, in execution order: head, whole tiles, tail

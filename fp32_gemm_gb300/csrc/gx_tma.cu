@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         dev::mbar_init(head_stored, 1);
         dev::mbar_init(epoch_known, 1);
         dev::fence_mbar_init();
-        *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G);
+        *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G, p.stream_kappa);
     }
     __syncthreads();
     if (vt == 0) trace_at(p, 0);

@@ -1,15 +1,18 @@
 """The stream kernel's split of a step's (tile, j) work over the CTAs, checked on the CPU through the library's own
 host copy of the code the kernel runs (sdm_gx_gemm_stream_piece). For every shape: each tile's j range 0..C-1 is
 covered exactly once, either whole by one CTA or as a head [0, s) on CTA b and a tail [s, C) on CTA b + 1; a CTA runs
-at most one head (first) and one tail (last); the CTAs' work differs by at most one unit; and, at equal rates, CTA b
-reaches its tail no earlier than CTA b - 1 has finished the matching head, so the hand-off never waits on work that
-has not started."""
+at most one head (first) and one tail (last); the CTAs' work differs by at most one unit, or, where the split charges
+each tile boundary inside a range KAPPA units of cost (steps of at least C + 2 KAPPA units per CTA), by at most
+2 KAPPA + 1 with the ranges that hold more boundaries the shorter; and, at equal rates, CTA b reaches its tail no
+earlier than CTA b - 1 has finished the matching head, so the hand-off never waits on work that has not started."""
 
 import random
 
 import pytest
 
 gx = pytest.importorskip("fp32_gemm_gb300")
+
+KAPPA = 12   # the library's charge per tile boundary of the split (applied when ntiles * C / G >= C + 2 KAPPA)
 
 SHAPES = [(256, 128, 152), (160, 100, 152), (152, 128, 152), (153, 128, 152), (303, 128, 152), (1000, 7, 152),
           (200, 1, 152), (4096, 256, 152), (5, 3, 5), (7, 64, 3), (1, 1, 1), (300, 96, 148)]
@@ -43,7 +46,8 @@ def _check(ntiles, C, G):
             done += j1 - j0
         per_cta.append(done)
     assert sum(per_cta) == ntiles * C
-    assert max(per_cta) - min(per_cta) <= 1
+    charged = ntiles * C // G >= C + 2 * KAPPA
+    assert max(per_cta) - min(per_cta) <= (2 * KAPPA + 1 if charged else 1)
     for t in range(ntiles):
         spans = sorted(cover[t])
         assert spans[0][0] == 0 and spans[-1][1] == C
@@ -60,6 +64,17 @@ def _check(ntiles, C, G):
 @pytest.mark.parametrize("shape", SHAPES)
 def test_stream_split_invariants(shape):
     _check(*shape)
+
+
+def test_large_step_charges_the_extra_piece():
+    """The large step (256 tiles of 128 x 128 on 152 CTAs, 215.6 units each): CTAs with three pieces (head, whole
+    tile, tail) take fewer units than those with two, by about the charge."""
+    units = {2: [], 3: []}
+    for b in range(152):
+        pcs = gx.stream_pieces(256, 128, 152, b)
+        units.setdefault(len(pcs), []).append(sum(j1 - j0 for (_, j0, j1, _) in pcs))
+    assert units[2] and units[3]
+    assert max(units[3]) < min(units[2]) + KAPPA and sum(units[3]) / len(units[3]) < sum(units[2]) / len(units[2]) - 4
 
 
 def test_stream_split_random_shapes():
