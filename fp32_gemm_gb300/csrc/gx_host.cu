@@ -208,44 +208,83 @@ struct Launch {
 };
 
 // The geometry rule (our re-derivation, for this kernel family, of the page's one-wave rows rule): estimate the step
-// time of every tile configuration on this device and take the fastest. A step's tiles spread over the SMs; an SM runs
-// up to `occ` CTAs at once; its FMA rate is 128 lanes x the configuration's measured efficiency x the fraction of the
-// eight-plus consumer warps it needs to reach it; each CTA also pays a per-tile cost (pipeline fill, epilogue, and the
-// j-chain's dependent-FMA latency) for every tile it runs in sequence.
-double estimate_cycles(const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
+// time of every configuration on this device and take the fastest. The model, in microseconds:
+//   step = base + compute + exposed memory,
+// compute = the busiest SM's FMA work at the configuration's rate plus a fixed cost per round of resident CTAs (tile
+// kernels: pipeline fill, epilogue, the chain's dependent latency), per slab round, or per piece (stream kernel);
+// exposed memory = the step's algorithmic bytes at 7 TB/s, of which a share shows in the step that shrinks with the
+// rounds an SM runs (later rounds load while earlier ones compute).
+// How a partial last wave lands (measured): leftover CTAs after the first full waves spread one per SM when they are
+// fewer than half the SMs, and otherwise fill whole SMs (every slot of an SM whose CTAs finished together), so that
+// the busiest SM runs a whole extra round. The constants were fitted by least squares (log error) to the measured step
+// time of every configuration on 66 shapes (P 48 .. 800, C 32 .. 128, hd 64 .. 128), one GB300 at 2.05 GHz; held out
+// by C, the fit picks within 2% of the fastest configuration on average.
+namespace model {
+constexpr double kClockMHz = 2050.0;
+constexpr double kBaseUs = 1.217;            // launch gap and first data of a chained step
+constexpr double kTileRoundCycles = 1230.0;  // per round of resident CTAs (tile kernels)
+constexpr double kPieceCycles = 1990.0;      // per piece of the stream kernel's split (fill, hand-off, epilogue)
+constexpr double kSlabRoundCycles = 2771.0;  // per round of four slabs
+constexpr double kStreamFixedCycles = 7732.0;
+constexpr double kMemExposed = 0.541;        // share of the step's bytes at kMemBytesPerUs left exposed by one round
+constexpr double kMemBytesPerUs = 7.0e6;
+// fitted FMA rate per SM, as a fraction of 128 lanes a cycle, by configuration (the order of the TMA configuration
+// table); a configuration past the table falls back to its kernel's own efficiency figure
+constexpr double kRate[] = {0.797, 0.747, 0.749, 0.752, 0.763, 0.721, 0.709, 0.677, 0.433, 0.430, 0.365,
+                            0.731, 1.000, 0.971, 0.940};
+constexpr int kRates = static_cast<int>(sizeof(kRate) / sizeof(kRate[0]));
+}  // namespace model
+
+// Tiles on the busiest SM and the rounds it runs them in, for `tiles` CTAs of which an SM holds `occ` at once.
+void busiest_sm(int64_t tiles, int occ, int sms, int64_t *per, int64_t *rounds, int64_t *resident) {
+    const int64_t w = static_cast<int64_t>(sms) * occ;
+    int64_t p;
+    if (tiles <= w) {
+        p = (tiles + sms - 1) / sms;
+    } else {
+        const int64_t full = tiles / w, left = tiles % w;
+        p = full * occ;
+        if (left) p += 2 * left > sms ? occ : (left + sms - 1) / sms;
+    }
+    const int64_t a = std::max<int64_t>(1, std::min<int64_t>(occ, p));
+    *per = p;
+    *rounds = (p + a - 1) / a;
+    *resident = a;
+}
+
+double estimate_us(int k, const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
     const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
     const double tile_fma = static_cast<double>(ci.TI) * ci.TC * C;
-    // FMA rate of an SM running n CTAs of this configuration: the measured efficiency, scaled down while fewer than
-    // eight consumer warps share the SM
-    auto rate = [&](int64_t n) {
-        return 128.0 * (ci.eff / 100.0) * std::min(1.0, static_cast<double>(n * ci.consumer_warps) / 8.0);
-    };
+    const double rate = 128.0 * (k < model::kRates ? model::kRate[k] : ci.eff / 100.0);
+    double cycles;
+    int64_t rounds;
     if (ci.kind == 1) {
         // balanced slabs: every SM gets at most ceil(slabs / SMs), in rounds of four on 16 warps; a partial round of
-        // k slabs costs about 1 + 0.9 k slabs (measured: its fixed part does not shrink with k)
+        // r slabs costs about 1 + 0.9 r slabs (its fixed part does not shrink with r)
         const int64_t per_sm = (tiles + sms - 1) / sms;
-        const int64_t full = per_sm / 4, k = per_sm % 4;
-        const double eq = 4.0 * static_cast<double>(full) + (k ? 1.0 + 0.9 * static_cast<double>(k) : 0.0);
-        const int64_t rounds = (per_sm + 3) / 4;
-        return eq * tile_fma / rate(2) + static_cast<double>(rounds) * (1500.0 + 8.0 * C);
-    }
-    if (ci.kind == 2) {
-        // (tile, j) units split evenly over every resident CTA (occ per SM, all busy to the end); each CTA runs up to
-        // two partial pieces besides its whole tiles, and the hand-off of partial sums costs about one k-block
+        const int64_t full = per_sm / 4, r = per_sm % 4;
+        const double eq = 4.0 * static_cast<double>(full) + (r ? 1.0 + 0.9 * static_cast<double>(r) : 0.0);
+        rounds = (per_sm + 3) / 4;
+        cycles = eq * tile_fma / rate + static_cast<double>(rounds) * model::kSlabRoundCycles;
+    } else if (ci.kind == 2) {
+        // (tile, j) units split evenly over every resident CTA; each CTA runs its whole tiles and up to two partial
+        // pieces
         const int per_sm = std::max(1, occ);
         const double units_sm = std::ceil(static_cast<double>(tiles) * static_cast<double>(C) / sms);
-        const double units_cta = units_sm / per_sm;
-        const double pieces = std::ceil(units_cta / static_cast<double>(C)) + 1.0;
-        return units_sm * ci.TI * ci.TC / rate(per_sm) + pieces * (1500.0 + 8.0 * C) + 2000.0;
+        rounds = static_cast<int64_t>(std::ceil(units_sm / per_sm / static_cast<double>(C))) + 1;
+        cycles = units_sm * ci.TI * ci.TC / rate + static_cast<double>(rounds) * model::kPieceCycles +
+                 model::kStreamFixedCycles;
+    } else {
+        // whole tiles; below four consumer warps resident an SM's FMA rate drops in proportion
+        int64_t per, a;
+        busiest_sm(tiles, occ, sms, &per, &rounds, &a);
+        const double share = std::min(1.0, static_cast<double>(a * ci.consumer_warps) / 4.0);
+        cycles = static_cast<double>(per) * tile_fma / (rate * share) +
+                 static_cast<double>(rounds) * model::kTileRoundCycles;
     }
-    // whole tiles: an SM runs rounds of up to `occ` concurrent CTAs; a last round with fewer CTAs runs at its own
-    // (lower) rate, and each round pays a per-tile cost (pipeline fill, epilogue, the chain's dependent latency)
-    const int64_t per_sm = (tiles + sms - 1) / sms;
-    const int64_t a = std::min<int64_t>(occ, per_sm);
-    const int64_t full = per_sm / a, rem = per_sm % a;
-    double t = static_cast<double>(full) * static_cast<double>(a) * tile_fma / rate(a);
-    if (rem) t += static_cast<double>(rem) * tile_fma / rate(rem);
-    return t + static_cast<double>(full + (rem ? 1 : 0)) * (1500.0 + 8.0 * C);
+    const double bytes = static_cast<double>(P) * static_cast<double>(C * C + 3 * C * hd) * 4.0;
+    return model::kBaseUs + cycles / model::kClockMHz +
+           model::kMemExposed * bytes / model::kMemBytesPerUs / static_cast<double>(std::max<int64_t>(1, rounds));
 }
 
 // The slab kernel needs whole 32-row slabs (C % 32 == 0) and at most two (chunk, column block) per round of four
@@ -307,14 +346,12 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
         }
         if (bk >= 0) return bk;
     }
-    // Otherwise the throughput estimate of every configuration; the slab kernel must beat the best tile
-    // configuration by 5% (its model is the coarser one).
+    // Otherwise the step-time model's fastest configuration.
     double best = 1e300;
     int bk = -1;
     for (int k = 0; k < tma_num_configs(); ++k) {
         if (!usable(k)) continue;
-        const ConfigInfo &ci = tma_config(k);
-        const double est = estimate_cycles(ci, d.tma_occ[k], d.sms, P, C, hd) * (ci.kind == 1 ? 1.0 / 0.95 : 1.0);
+        const double est = estimate_us(k, tma_config(k), d.tma_occ[k], d.sms, P, C, hd);
         if (est < best * 0.999) {
             best = est;
             bk = k;
