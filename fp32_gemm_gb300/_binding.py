@@ -429,7 +429,7 @@ def kernel_attrs(path: int, config: int) -> dict:
     return {"regs": out[0], "local_bytes": out[1], "static_smem": out[2], "max_threads": out[3]}
 
 
-CONFIG_KINDS = {0: "tile", 1: "slab", 2: "stream"}
+CONFIG_KINDS = {0: "tile", 1: "slab", 2: "stream", 3: "offset"}
 
 
 def config_info(path: int, config: int) -> dict:

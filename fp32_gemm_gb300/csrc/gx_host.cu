@@ -186,16 +186,31 @@ sdm_gx_strides contiguous(int64_t C, int64_t hd) {
     return s;
 }
 
-bool tma_eligible(const float *du, const float *x, const float *dv, const sdm_gx_strides &s) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(du) | reinterpret_cast<uintptr_t>(x) |
-                        reinterpret_cast<uintptr_t>(dv);
-    if (a & 15u) return false;
+// Strides a tensor map can describe: multiples of 16 bytes, below 2^40 bytes.
+bool tma_strides_ok(const sdm_gx_strides &s) {
     const int64_t st = s.x_sn | s.x_sj | s.dv_sn | s.dv_sj | s.du_sn | s.du_si;
     if (st & 3) return false;
-    // tensor-map strides are in bytes and must stay below 2^40
     const int64_t mx = std::max({s.x_sn, s.x_sj, s.dv_sn, s.dv_sj, s.du_sn, s.du_si});
     return mx * 4 < kMaxStride;
 }
+
+// The TMA kernels proper: every base on a 16-byte boundary.
+bool tma_eligible(const float *du, const float *x, const float *dv, const sdm_gx_strides &s) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(du) | reinterpret_cast<uintptr_t>(x) |
+                        reinterpret_cast<uintptr_t>(dv);
+    return (a & 15u) == 0 && tma_strides_ok(s);
+}
+
+// The offset configurations: TMA strides, some base 4, 8 or 12 bytes past a 16-byte boundary (every base is 4-byte
+// aligned after validate()).
+bool tma_offset_eligible(const float *du, const float *x, const float *dv, const sdm_gx_strides &s) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(du) | reinterpret_cast<uintptr_t>(x) |
+                        reinterpret_cast<uintptr_t>(dv);
+    return (a & 15u) != 0 && tma_strides_ok(s);
+}
+
+// floats by which p lies past a 16-byte boundary (0..3)
+int32_t floats_off(const void *p) { return static_cast<int32_t>((reinterpret_cast<uintptr_t>(p) & 15u) / 4u); }
 
 // ---- the launch description ----------------------------------------------------------------------------------------
 struct Launch {
@@ -231,7 +246,7 @@ constexpr double kMemBytesPerUs = 7.0e6;
 // fitted FMA rate per SM, as a fraction of 128 lanes a cycle, by configuration (the order of the TMA configuration
 // table); a configuration past the table falls back to its kernel's own efficiency figure
 constexpr double kRate[] = {0.797, 0.747, 0.749, 0.752, 0.763, 0.721, 0.709, 0.677, 0.433, 0.430, 0.365,
-                            0.731, 1.000, 0.971, 0.940};
+                            0.731, 1.000, 0.971, 0.940, 0.565, 0.480, 0.630, 0.305};
 constexpr int kRates = static_cast<int>(sizeof(kRate) / sizeof(kRate[0]));
 }  // namespace model
 
@@ -253,7 +268,8 @@ void busiest_sm(int64_t tiles, int occ, int sms, int64_t *per, int64_t *rounds, 
 }
 
 double estimate_us(int k, const ConfigInfo &ci, int occ, int sms, int64_t P, int64_t C, int64_t hd) {
-    const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+    const int64_t g = ci.kind == 3 && ci.shifted ? 3 : 0;   // the shifted grid's extra rows and columns, at most
+    const int64_t tiles = P * ((C + g + ci.TI - 1) / ci.TI) * ((hd + g + ci.TC - 1) / ci.TC);
     const double tile_fma = static_cast<double>(ci.TI) * ci.TC * C;
     const double rate = 128.0 * (k < model::kRates ? model::kRate[k] : ci.eff / 100.0);
     double cycles;
@@ -307,15 +323,19 @@ int stream_ctas_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_
 // stream_ctas_only > 0: a stream configuration is admitted only if its split runs exactly that many CTAs (the shared
 // static workspace of sdm_gx_gemm_step_noalloc, whose per-CTA launch counters stay equal only if every launch on it
 // counts the same CTAs).
+// offset: some operand base lies off a 16-byte boundary; only the offset configurations (kind 3) serve it, and only
+// it takes them unless forced.
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes,
-                      int stream_ctas_only) {
+                      int stream_ctas_only, bool offset = false) {
     if (forced >= 0) return forced;
     auto tiles_of = [&](const ConfigInfo &ci) {
-        return P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
+        const int64_t g = ci.kind == 3 && ci.shifted ? 3 : 0;   // the shifted grid's extra rows and columns, at most
+        return P * ((C + g + ci.TI - 1) / ci.TI) * ((hd + g + ci.TC - 1) / ci.TC);
     };
     auto usable = [&](int k) {
         const ConfigInfo &ci = tma_config(k);
-        return d.tma_occ[k] >= 1 && config_eligible(ci, P, C, hd, stream_ctas_of(d, k), ws_bytes) &&
+        return d.tma_occ[k] >= 1 && (ci.kind == 3) == offset &&
+               config_eligible(ci, P, C, hd, stream_ctas_of(d, k), ws_bytes) &&
                !(ci.kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) &&
                !(ci.kind == 1 && !d.slab_ok) && tiles_of(ci) < kTwo31;
     };
@@ -422,7 +442,9 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     const int forced = static_cast<int>(flags & SDM_GX_FLAG_CONFIG_MASK) - 1;
     const int forced_occ = static_cast<int>((flags & SDM_GX_FLAG_CTAS_MASK) >> SDM_GX_FLAG_CTAS_SHIFT);
     const bool x_t = (flags & SDM_GX_FLAG_X_TRANSPOSED) != 0;   // x stored [n][i][j]: the generic kernels
-    const bool use_tma = !(flags & SDM_GX_FLAG_GENERIC) && !x_t && tma_eligible(du, x, dv, s);
+    const bool tma_ok = !(flags & SDM_GX_FLAG_GENERIC) && !x_t;
+    const bool offs = tma_ok && !tma_eligible(du, x, dv, s) && tma_offset_eligible(du, x, dv, s);
+    const bool use_tma = tma_ok && (offs || tma_eligible(du, x, dv, s));
     Launch l;
     l.device = dev;
     l.n_first = n_first;
@@ -434,10 +456,12 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     int occ = 0;
     if (use_tma) {
         if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
-        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, stream_ctas_only);
+        const int k =
+            choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, stream_ctas_only, offs);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
-        if (!config_eligible(*ci, sh.P, sh.C, sh.hd, stream_ctas_of(d, k), ws != nullptr ? ws_bytes : 0) ||
+        if ((offs && ci->kind != 3) ||
+            !config_eligible(*ci, sh.P, sh.C, sh.hd, stream_ctas_of(d, k), ws != nullptr ? ws_bytes : 0) ||
             (ci->kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) ||
             (ci->kind == 1 && !d.slab_ok))
             return SDM_GX_E_FLAGS;
@@ -449,11 +473,21 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         std::memset(&t, 0, sizeof(t));
         CUresult r;
         const int du_rows = ci->kind == 1 ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
-        if ((r = encode_map(&t.tm_x, x0, sh.C, sh.C, n_count, s.x_sj, s.x_sn, ci->TI, ci->KB)) != CUDA_SUCCESS ||
-            (r = encode_map(&t.tm_dv, dv0, sh.hd, sh.C, n_count, s.dv_sj, s.dv_sn, ci->TC, ci->KB)) !=
+        // offset configurations: each map from its base rounded down to 16 bytes, the innermost extent grown by the
+        // offset; element-load ones take boxes 4 floats wider (the tile from float off of each box row on), shifted-
+        // grid ones the tile's own x and d_dv boxes and a d_u box 8 floats wider
+        const bool k3 = ci->kind == 3, shifted = k3 && ci->shifted;
+        const int ox = k3 ? floats_off(x0) : 0, ov = k3 ? floats_off(dv0) : 0, ou = k3 ? floats_off(du0) : 0;
+        const int wide = k3 && !shifted ? 4 : 0, wide_u = shifted ? 8 : wide;
+        t.off_x = ox;
+        t.off_v = ov;
+        t.off_u = ou;
+        if ((r = encode_map(&t.tm_x, x0 - ox, sh.C + ox, sh.C, n_count, s.x_sj, s.x_sn, ci->TI + wide, ci->KB)) !=
                 CUDA_SUCCESS ||
-            (r = encode_map(&t.tm_du, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, du_rows)) !=
-                CUDA_SUCCESS ||
+            (r = encode_map(&t.tm_dv, dv0 - ov, sh.hd + ov, sh.C, n_count, s.dv_sj, s.dv_sn, ci->TC + wide,
+                            ci->KB)) != CUDA_SUCCESS ||
+            (r = encode_map(&t.tm_du, du0 - ou, sh.hd + ou, sh.C, n_count, s.du_si, s.du_sn, ci->TC + wide_u,
+                            du_rows)) != CUDA_SUCCESS ||
             (ci->kind == 1 &&
              ((r = encode_x_slabs(&t.tm_x4, x0, sh.C, n_count, s.x_sj, s.x_sn, ci->KB)) != CUDA_SUCCESS ||
               (r = encode_map(&t.tm_du1, du0, sh.hd, sh.C, n_count, s.du_si, s.du_sn, ci->TC, ci->TI)) !=
@@ -465,8 +499,8 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         t.P = static_cast<int32_t>(sh.P);
         t.C = static_cast<int32_t>(sh.C);
         t.hd = static_cast<int32_t>(sh.hd);
-        t.nib = static_cast<int32_t>((sh.C + ci->TI - 1) / ci->TI);
-        t.ncb = static_cast<int32_t>((sh.hd + ci->TC - 1) / ci->TC);
+        t.nib = static_cast<int32_t>((sh.C + (shifted ? ox : 0) + ci->TI - 1) / ci->TI);
+        t.ncb = static_cast<int32_t>((sh.hd + (shifted ? ov : 0) + ci->TC - 1) / ci->TC);
         const int64_t tiles = sh.P * t.nib * t.ncb;
         if (tiles >= kTwo31) return SDM_GX_E_GRID;
         t.ntiles = static_cast<int32_t>(tiles);

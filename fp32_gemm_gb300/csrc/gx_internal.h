@@ -39,6 +39,9 @@ struct TmaParams {
     int32_t stall_test;     // 1: the producer withholds the first stage's copies (failure-detection test hook)
     int32_t handoff_test;   // 1: stream kernel: publishers store but never flag their partial sums (test hook)
     int32_t stream_kappa;   // stream kernel: the split's charge per tile boundary in a CTA's range (stream_kappa())
+    // offset configurations (kind 3): floats (0..3) by which the rows of x, d_dv and d_u start past the 16-byte
+    // boundary their tensor maps were encoded from
+    int32_t off_x, off_v, off_u;
     // Optional per-CTA timeline (nullptr: off; tile and stream kernels). Launch li = n_base / P < trace_launches writes,
     // for its CTA b of G, four global-timer stamps (ns) at trace[(li * G + b) * 4 + k]: k = 0 the CTA's start, 1 its
     // consumer warp 0 past the dependency wait, 2 that warp holding its first staged data, 3 that warp done with its
@@ -69,7 +72,10 @@ struct ConfigInfo {
     int TI, TC, KB, stages, threads, smem, RM, RN, consumer_warps;
     int eff;    // measured FMA-pipe efficiency (percent) with every SM busy
     int kind;   // 0: tile kernel; 1: balanced slab kernel (TI = slab rows; needs C % TI == 0 and C / TI >= 3);
-                // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace)
+                // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace);
+                // 3: tile kernel for operand bases off a 16-byte boundary (aligned-down tensor maps)
+    int shifted;   // kind 3: 0 element loads of boxes 4 floats wider; 1 tiles on the shifted grid
+                   // (ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles a chunk, a d_u box 8 floats wider)
 };
 
 // Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,

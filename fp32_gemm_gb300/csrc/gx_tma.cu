@@ -37,6 +37,8 @@ struct TCfg {
     static constexpr int SLAB = 0;
     static constexpr bool ROWS_OUTER = false;      // FMA order within one j: column-outer (see chain_j)
     static constexpr bool DUPRE = false;           // stream kernel only: d_u read into registers in the last stage
+    static constexpr bool ELEM = false;            // offset configurations (OCfg): element loads of wide boxes
+    static constexpr bool SHIFT = false;           // offset configurations (OCfg): tiles on the shifted grid
     static constexpr int RM = RM_, RN = RN_;       // per-thread tile: rows x columns
     static constexpr int WM = WM_, WN = WN_;       // consumer warps along rows / columns
     static constexpr int KB = KB_, ST = ST_;       // j rows per stage, stages
@@ -48,6 +50,7 @@ struct TCfg {
     static constexpr int TC = WN * RN * LN;
     static constexpr int NCW = WM * WN;
     static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr int XP = TI, DP = TC, UP = TC;   // row pitches (floats) of the staged x, d_dv and d_u boxes
     // every TMA destination starts on a 128-byte boundary (the dynamic shared window is aligned up to 128 bytes)
     static constexpr int XS_BYTES = align_up(KB * TI * 4, 128);
     static constexpr int DS_BYTES = align_up(KB * TC * 4, 128);
@@ -99,6 +102,18 @@ __device__ __forceinline__ Tile decode_tile(const TmaParams &p, int t) {
     return Tile{p.n_base + pp, ib * Cfg::TI, cb * Cfg::TC};
 }
 
+// V consecutive floats of a staged box: one vector load, or V element loads where the box rows sit one to three
+// floats off a 16-byte boundary (the offset configurations).
+template <class Cfg, int V>
+__device__ __forceinline__ void lds(const float *p, float *o) {
+    if constexpr (Cfg::ELEM) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] = p[e];
+    } else {
+        dev::Vec<V>::load(p, o);
+    }
+}
+
 // One j of the chain: the thread's x and d_dv fragments of row jj, then its RM x RN FMAs.
 template <class Cfg>
 __device__ __forceinline__ void chain_j(const float *__restrict__ xs, const float *__restrict__ ds, int jj,
@@ -106,9 +121,9 @@ __device__ __forceinline__ void chain_j(const float *__restrict__ xs, const floa
                                         float (&acc)[Cfg::RM][Cfg::RN]) {
     float a[Cfg::RM], b[Cfg::RN];
 #pragma unroll
-    for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
+    for (int s = 0; s < Cfg::SR; ++s) lds<Cfg, Cfg::VR>(xs + jj * Cfg::XP + ro[s], a + s * Cfg::VR);
 #pragma unroll
-    for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+    for (int s = 0; s < Cfg::SN; ++s) lds<Cfg, Cfg::VN>(ds + jj * Cfg::DP + co[s], b + s * Cfg::VN);
     if constexpr (Cfg::RM % 2 == 0 && Cfg::ROWS_OUTER) {
         // rows in pairs, one row pair against all of the thread's columns before the next pair: the packed x pair
         // stays the same over RN consecutive FMAs (with 8 x 8 thread tiles the FMA pipe measured 89-90% busy inside
@@ -166,9 +181,9 @@ __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const 
         for (int jj = 0; jj < cnt; ++jj) {
             float a[Cfg::RM], b[Cfg::RN];
 #pragma unroll
-            for (int s = 0; s < Cfg::SR; ++s) dev::Vec<Cfg::VR>::load(xs + jj * Cfg::TI + ro[s], a + s * Cfg::VR);
+            for (int s = 0; s < Cfg::SR; ++s) lds<Cfg, Cfg::VR>(xs + jj * Cfg::XP + ro[s], a + s * Cfg::VR);
 #pragma unroll
-            for (int s = 0; s < Cfg::SN; ++s) dev::Vec<Cfg::VN>::load(ds + jj * Cfg::TC + co[s], b + s * Cfg::VN);
+            for (int s = 0; s < Cfg::SN; ++s) lds<Cfg, Cfg::VN>(ds + jj * Cfg::DP + co[s], b + s * Cfg::VN);
             if constexpr (Cfg::RM % 2 == 0) {
                 // rows in pairs: (acc[r][c], acc[r+1][c]) += (a[r], a[r+1]) * (b[c], b[c]) with one packed FMA
 #pragma unroll
@@ -189,33 +204,44 @@ __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const 
 }
 
 // Epilogue: d_u + acc with one rounding each (the staged d_u tile us[TI][TC]), stored straight to global memory with
-// vector stores; a vector that straddles hd is stored element by element; rows >= C and columns >= hd are skipped.
+// vector stores; a vector that straddles hd, or one whose d_u address is off a 16-byte boundary (offset
+// configurations), is stored element by element; rows outside 0..C-1 and columns outside 0..hd-1 are skipped.
+// Shifted-grid configurations: the tile's output rows and columns start off_x and off_v before its box coordinates,
+// and us points at the tile's first column inside the wider d_u box (vector reads when off_u == off_v).
 template <class Cfg>
 __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, const float *us, const int (&ro)[Cfg::SR],
                                          const int (&co)[Cfg::SN], const float (&acc)[Cfg::RM][Cfg::RN]) {
+    const int ir0 = Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0;
+    const int cr0 = Cfg::SHIFT ? tl.c0 - p.off_v : tl.c0;
+    const bool vec = !Cfg::ELEM && (!Cfg::SHIFT || p.off_u == p.off_v);
 #pragma unroll
     for (int sr = 0; sr < Cfg::SR; ++sr) {
 #pragma unroll
         for (int er = 0; er < Cfg::VR; ++er) {
             const int rl = ro[sr] + er;
-            const int i = tl.i0 + rl;
-            if (i >= p.C) continue;
+            const int i = ir0 + rl;
+            if (i >= p.C || (Cfg::SHIFT && i < 0)) continue;
             float *grow = p.du + static_cast<int64_t>(tl.n) * p.du_sn + static_cast<int64_t>(i) * p.du_si;
 #pragma unroll
             for (int sc = 0; sc < Cfg::SN; ++sc) {
                 const int cl = co[sc];
-                const int c = tl.c0 + cl;
-                if (c >= p.hd) continue;
+                const int c = cr0 + cl;
+                if (c >= p.hd || (Cfg::SHIFT && c + Cfg::VN <= 0)) continue;
                 float u[Cfg::VN], o[Cfg::VN];
-                dev::Vec<Cfg::VN>::load(us + rl * Cfg::TC + cl, u);
+                if (vec) {
+                    dev::Vec<Cfg::VN>::load(us + rl * Cfg::UP + cl, u);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < Cfg::VN; ++e) u[e] = us[rl * Cfg::UP + cl + e];
+                }
 #pragma unroll
                 for (int e = 0; e < Cfg::VN; ++e) o[e] = __fadd_rn(u[e], acc[sr * Cfg::VR + er][sc * Cfg::VN + e]);
-                if (c + Cfg::VN <= p.hd) {
+                if (vec && c >= 0 && c + Cfg::VN <= p.hd) {
                     dev::Vec<Cfg::VN>::store(grow + c, o);
                 } else {
 #pragma unroll
                     for (int e = 0; e < Cfg::VN; ++e)
-                        if (c + e < p.hd) grow[c + e] = o[e];
+                        if (c + e >= 0 && c + e < p.hd) grow[c + e] = o[e];
                 }
             }
         }
@@ -227,7 +253,7 @@ template <class Cfg, int V>
 __device__ __forceinline__ void load_du_vec(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
                                             float (&u)[Cfg::RM][Cfg::RN]) {
     constexpr int sr = V / (Cfg::VR * Cfg::SN), er = (V / Cfg::SN) % Cfg::VR, sc = V % Cfg::SN;
-    dev::Vec<Cfg::VN>::load(us + (ro[sr] + er) * Cfg::TC + co[sc], &u[sr * Cfg::VR + er][sc * Cfg::VN]);
+    lds<Cfg, Cfg::VN>(us + (ro[sr] + er) * Cfg::UP + co[sc], &u[sr * Cfg::VR + er][sc * Cfg::VN]);
 }
 
 template <class Cfg, int... V>
@@ -295,6 +321,14 @@ __device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl
     }
 }
 
+// Coordinates of a tile's d_u box: the tile's own, or on the shifted grid 4 floats before its column coordinate (an
+// aligned x; the box is 8 floats wider than the tile) and off_x rows before its row coordinate (the tile's first output
+// row; a negative row or column coordinate reads zeros).
+template <class Cfg>
+__device__ __forceinline__ int du_x(const Tile &tl) { return Cfg::SHIFT ? tl.c0 - 4 : tl.c0; }
+template <class Cfg>
+__device__ __forceinline__ int du_y(const TmaParams &p, const Tile &tl) { return Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0; }
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const __grid_constant__ TmaParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 for (int kb = 0; kb < nk; ++kb) dev::tma_prefetch_3d(&p.tm_dv, tl.c0, kb * Cfg::KB, tl.n);
             }
             dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
-            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(tl), du_y<Cfg>(p, tl), tl.n, du_full);
             du_issued = 1;
         }
         dev::grid_dependency_wait();
@@ -384,7 +418,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                     break;
                 }
                 dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
-                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, tl.c0, tl.i0, tl.n, du_full);
+                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(tl), du_y<Cfg>(p, tl), tl.n, du_full);
                 ++du_issued;
             }
         }
@@ -419,7 +453,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
 
     dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
     if (threadIdx.x == 0) trace_at(p, 1);
-    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U);
+    // element-load offset configurations: the wide boxes hold the tile from float off on; shifted-grid ones: the
+    // d_u box starts 4 floats before the tile's box coordinate, and the tile's columns off_u - off_v after that
+    const int ox = Cfg::ELEM ? p.off_x : 0, ov = Cfg::ELEM ? p.off_v : 0;
+    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) +
+                            (Cfg::ELEM ? p.off_u : (Cfg::SHIFT ? 4 + p.off_u - p.off_v : 0));
     int it = 0;
     int tk = 0;
     for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x), ++tk) {
@@ -439,8 +477,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 return;
             }
 
-            const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
-            const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
+            const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES) + ox;
+            const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES) + ov;
             const int nj = p.C - kb * Cfg::KB;
             if (nj >= Cfg::KB) {
                 chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
@@ -485,6 +523,8 @@ struct SCfg {
     static constexpr int TC = WN * RN * LN;        // 128 columns
     static constexpr int NCW = WS * WN;            // 16 consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
+    static constexpr bool ELEM = false, SHIFT = false;
+    static constexpr int XP = TI, DP = TC, UP = TC;
     static constexpr int X_SLAB = KB * TI * 4;     // bytes of one slab's x rows per stage
     static constexpr int D_BOX = KB * TC * 4;
     static constexpr int U_SLAB = TI * TC * 4;
@@ -1153,7 +1193,7 @@ const void *kernel_of() {
 template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF, Cfg::SLAB};
+                      Cfg::EFF, (Cfg::ELEM || Cfg::SHIFT) ? 3 : Cfg::SLAB, Cfg::SHIFT ? 1 : 0};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
@@ -1179,6 +1219,43 @@ using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128
 // the large step comes out even (22.3 us per step either way). The rule prefers C12; autotune measures both.
 using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
 
+// The tile kernel for operands whose rows start 4, 8 or 12 bytes past a 16-byte boundary (a 4-byte-aligned base with
+// strides that are multiples of 16 bytes: a slice at an odd offset, say). TMA needs 16-byte-aligned bases and innermost
+// coordinates, so the host encodes each operand's map from its base rounded down to 16 bytes, with the innermost
+// extent grown by the offset (off = 1..3 floats; the map's rows then overlap the previous row's last off floats, which
+// are loaded and never used). Two ways to use such maps:
+//   * element loads (SHIFT_ = false): every box is 4 floats wider than the tile, so that a box at the tile's own
+//     (aligned) coordinate holds the tile's columns from float off on; the consumers read the staged boxes at that
+//     offset with element loads (vectors would straddle 16-byte boundaries) and store d_u element by element. The
+//     tiles are the aligned kernel's; the chain's shared loads are four times as many.
+//   * the shifted grid (SHIFT_ = true): tiles are cut on the aligned-down maps' own grid, so tile (ib, cb) holds output
+//     rows ib TI - off_x .. and columns cb TC - off_v .., x and d_dv boxes are the tile's own size and the chain is the
+//     aligned kernel's, vector loads included; a step has ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles per
+//     chunk (rows and columns outside the operands are computed on zeros and not stored). The d_u box is 8 floats
+//     wider, from 4 floats before the tile's column coordinate, which covers the tile's columns for any off_u.
+// With every offset 0 either is the tile kernel on a few idle columns.
+template <class T, int EFF_, bool SHIFT_>
+struct OCfg : T {
+    static constexpr int EFF = EFF_;
+    static constexpr bool ELEM = !SHIFT_, SHIFT = SHIFT_;
+    static constexpr int XP = SHIFT_ ? T::TI : T::TI + 4, DP = SHIFT_ ? T::TC : T::TC + 4;
+    static constexpr int UP = SHIFT_ ? T::TC + 8 : T::TC + 4;
+    static constexpr int XS_BYTES = align_up(T::KB * XP * 4, 128);
+    static constexpr int DS_BYTES = align_up(T::KB * DP * 4, 128);
+    static constexpr int DU_BYTES = align_up(T::TI * UP * 4, 128);
+    static constexpr int OFF_D = T::ST * XS_BYTES;
+    static constexpr int OFF_U = OFF_D + T::ST * DS_BYTES;
+    static constexpr int OFF_BAR = OFF_U + DU_BYTES;
+    static constexpr int SMEM = OFF_BAR + align_up(T::NBAR * 8, 128) + 128;
+    static constexpr uint32_t STAGE_TX = static_cast<uint32_t>(T::KB * (XP + DP) * 4);
+    static constexpr uint32_t DU_TX = static_cast<uint32_t>(T::TI * UP * 4);
+    static_assert(XP <= 256 && DP <= 256, "TMA box dimensions are at most 256");
+};
+using C15 = OCfg<C0, 60, false>;   // 128 x 128, 16 warps, element loads: steps that fill the SMs
+using C16 = OCfg<C7, 50, false>;   //  32 x  64, 4 warps, element loads
+using C17 = OCfg<C7, 60, true>;    //  32 x  64, 4 warps, shifted grid
+using C18 = OCfg<C10, 20, true>;   //   8 x  32, 1 warp, shifted grid: the smallest steps
+
 struct Entry {
     ConfigInfo info;
     const void *fn;
@@ -1189,7 +1266,8 @@ struct Entry {
 const Entry kEntries[] = {SDMGX_ENTRY(C0), SDMGX_ENTRY(C1), SDMGX_ENTRY(C2), SDMGX_ENTRY(C3), SDMGX_ENTRY(C4),
                           SDMGX_ENTRY(C5), SDMGX_ENTRY(C6), SDMGX_ENTRY(C7), SDMGX_ENTRY(C8), SDMGX_ENTRY(C9),
                           SDMGX_ENTRY(C10), SDMGX_ENTRY(C11), SDMGX_ENTRY(C12), SDMGX_ENTRY(C13),
-                          SDMGX_ENTRY(C14)};
+                          SDMGX_ENTRY(C14), SDMGX_ENTRY(C15), SDMGX_ENTRY(C16), SDMGX_ENTRY(C17),
+                          SDMGX_ENTRY(C18)};
 #undef SDMGX_ENTRY
 
 }  // namespace

@@ -1,15 +1,16 @@
 """The plan's configuration choice on a described GB300-like device, without a GPU (sdm_gx_gemm_choose_config runs the
 same host rule as plan creation). The device: 152 SMs and the resident CTAs per SM of every configuration, both as a
-GB300 reports them through plan geometry (1 for the 128 x 128 tiles and the one-CTA stream configuration, 2 for the
-64-128-row tiles, 4 for 32 x 64 and 16 x 64, 10 for the one-warp tiles; generic 6, 4, 2, 2). The expected picks are
-the configurations measured fastest on a GB300 for these shapes."""
+GB300 reports them through plan geometry (1 for the 128 x 128 tiles, their offset variant and the one-CTA stream
+configuration, 2 for the 64-128-row tiles, 4 for 32 x 64 and 16 x 64 and both offset 32 x 64 variants, 10 for the
+one-warp tiles and the offset 8 x 32; generic 6, 4, 2, 2). The expected picks are the configurations measured fastest on a
+GB300 for these shapes."""
 
 import pytest
 
 gx = pytest.importorskip("fp32_gemm_gb300")
 
 SMS = 152
-TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2, 1]
+TMA_OCC = [1, 1, 2, 2, 2, 2, 2, 4, 4, 10, 10, 1, 1, 2, 1, 1, 4, 4, 10]
 GEN_OCC = [6, 4, 2, 2]
 WS = 64 << 20   # a plan workspace large enough for every stream configuration
 

@@ -140,7 +140,7 @@ def test_every_generic_config(config, shape):
 EDGE_VARIANTS = {
     "hd100": dict(hd=100, offset=0, row_pad=0, path=1),
     "hd99": dict(hd=99, offset=0, row_pad=0, path=0),
-    "hd128_misaligned": dict(hd=128, offset=1, row_pad=0, path=0),
+    "hd128_misaligned": dict(hd=128, offset=1, row_pad=0, path=1),   # an offset configuration (aligned-down maps)
     "hd128_ld129": dict(hd=128, offset=0, row_pad=1, path=0),
     "hd128_ld132": dict(hd=128, offset=0, row_pad=4, path=1),
 }
@@ -164,6 +164,63 @@ def test_edge_patterns(vset, variant):
     got = du.host()
     zero = (got == 0) & ~np.isnan(got)
     assert not np.any(np.signbit(got[zero])), "a -0 output"
+
+
+def _offset_configs():
+    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "offset"]
+
+
+OFFSET_PATTERNS = [(1, 1, 1), (2, 0, 3), (3, 2, 1), (0, 1, 0), (0, 0, 2)]   # floats past 16 bytes: d_u, x, d_dv
+
+
+@pytest.mark.parametrize("offs", OFFSET_PATTERNS)
+@pytest.mark.parametrize("shape", [(3, 100, 76), (2, 48, 128), (5, 12, 4)])
+def test_offset_bases_every_offset_config(shape, offs):
+    """Operand bases 4, 8 or 12 bytes past a 16-byte boundary, each operand its own offset: the plan takes an offset
+    configuration (TMA from aligned-down maps, boxes 4 floats wider), and every offset configuration, forced, gives the
+    oracle's bits, ragged in rows, columns and j, without touching the floats around the operands."""
+    P, C, hd = shape
+    w = synth.Workload("offset", 69, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [1, 0])
+    cfgs = _offset_configs()
+    assert cfgs
+    auto = None
+    for k in [None] + cfgs:
+        du = DevArray(inp["d_u"], offs[0])
+        dx, dv = DevArray(inp["x"], offs[1]), DevArray(inp["d_dv"], offs[2])
+        pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=0 if k is None else gx.config_flag(k))
+        g = pl.geometry()
+        assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"] == "offset", g
+        if k is None:
+            auto = g["config"]
+        pl.run(1, -1, pdl=True)
+        torch.cuda.synchronize()
+        assert_bitwise(du.host(), want, f"offset config {k if k is not None else auto} {shape} {offs}")
+        assert du.guards_intact() and dx.guards_intact() and dv.guards_intact()
+        _check_untouched(dx, dv, inp, f"offset config {k}")
+    # a configuration of the aligned kernels, forced on offset bases, is refused
+    du = DevArray(inp["d_u"], offs[0])
+    dx, dv = DevArray(inp["x"], offs[1]), DevArray(inp["d_dv"], offs[2])
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(0))
+    assert e.value.name == "SDM_GX_E_FLAGS"
+
+
+def test_offset_bases_large_shape():
+    """The large shape (P = 256, C = hd = 128) with every base 4 bytes past a 16-byte boundary: two full steps through
+    the plan's offset configuration, compared everywhere."""
+    w = synth.WORKLOADS["large"]
+    inp = synth.make_inputs(w, N=2 * w.P)
+    want, _ = _oracle_steps(inp, w.P, [0, 1])
+    du, dx, dv = _dev(inp, offset=1)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P)
+    g = pl.geometry()
+    assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"] == "offset", g
+    pl.run(pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, "large 2 steps, offset bases")
+    assert du.guards_intact() and dx.guards_intact() and dv.guards_intact()
 
 
 def test_producer_chain_full():
