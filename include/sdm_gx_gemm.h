@@ -16,6 +16,12 @@
  * as [N, C, hd] with d_dv[n, j, c] at d_dv[(n*C + j)*hd + c]; d_u is [N, C, hd] float32, updated in place. The
  * strided entry points take element strides instead (innermost stride always 1).
  *
+ * Kernels (the same bits on every one): strides that are multiples of 4 floats (16 bytes) take the TMA-fed path 1:
+ * its aligned configurations when every base pointer is 16-byte aligned, its offset configurations when some base is
+ * 4, 8 or 12 bytes past a 16-byte boundary (tensor maps encoded from the base rounded down, tiles read from the
+ * offset on). Other layouts (rows of a stride that is not a multiple of 4 floats) take the generic path 0, as does
+ * SDM_GX_FLAG_GENERIC.
+ *
  * Ownership: the caller owns every device buffer and stream. The library never allocates or frees device memory.
  * A plan holds raw device pointers and host memory only; it is valid while the buffers it names live. A plan created
  * with a workspace (sdm_gx_gemm_plan_create_ws) uses that caller-owned device buffer as scratch for as long as it lives.
@@ -97,7 +103,8 @@ typedef struct sdm_gx_geom {
     int32_t stages;       /* pipeline stages (TMA path) or 1                                                   */
     int32_t threads;      /* threads per CTA                                                                   */
     int32_t smem_bytes;   /* dynamic shared memory per CTA                                                     */
-    int64_t tiles;        /* tiles per step: P * ceil(C / TI) * ceil(hd / TC)                                   */
+    int64_t tiles;        /* tiles per step: P * ceil(C / TI) * ceil(hd / TC) (offset configurations on the
+                             shifted grid: P * ceil((C + off_x) / TI) * ceil((hd + off_dv) / TC), off in floats)  */
     int32_t ctas;         /* CTAs launched per step (persistent: each loops over tiles)                        */
     int32_t ctas_per_sm;  /* resident CTAs per SM at this configuration                                        */
     int32_t sms;          /* SM count of the device                                                            */
