@@ -475,10 +475,10 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         const int du_rows = ci->kind == 1 ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
         // offset configurations: each map from its base rounded down to 16 bytes, the innermost extent grown by the
         // offset; element-load ones take boxes 4 floats wider (the tile from float off of each box row on), shifted-
-        // grid ones the tile's own x and d_dv boxes and a d_u box 8 floats wider
+        // grid ones the tile's own x and d_dv boxes and a d_u box 4 floats wider
         const bool k3 = ci->kind == 3, shifted = k3 && ci->shifted;
         const int ox = k3 ? floats_off(x0) : 0, ov = k3 ? floats_off(dv0) : 0, ou = k3 ? floats_off(du0) : 0;
-        const int wide = k3 && !shifted ? 4 : 0, wide_u = shifted ? 8 : wide;
+        const int wide = k3 && !shifted ? 4 : 0, wide_u = k3 ? 4 : 0;
         t.off_x = ox;
         t.off_v = ov;
         t.off_u = ou;

@@ -321,11 +321,13 @@ __device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl
     }
 }
 
-// Coordinates of a tile's d_u box: the tile's own, or on the shifted grid 4 floats before its column coordinate (an
-// aligned x; the box is 8 floats wider than the tile) and off_x rows before its row coordinate (the tile's first output
-// row; a negative row or column coordinate reads zeros).
+// Coordinates of a tile's d_u box: the tile's own, or on the shifted grid off_x rows before its row coordinate (the
+// tile's first output row) and, when off_u < off_v, 4 floats before its column coordinate (an aligned x; the box is 4
+// floats wider than the tile); a negative row or column coordinate reads zeros.
 template <class Cfg>
-__device__ __forceinline__ int du_x(const Tile &tl) { return Cfg::SHIFT ? tl.c0 - 4 : tl.c0; }
+__device__ __forceinline__ int du_x(const TmaParams &p, const Tile &tl) {
+    return Cfg::SHIFT && p.off_u < p.off_v ? tl.c0 - 4 : tl.c0;
+}
 template <class Cfg>
 __device__ __forceinline__ int du_y(const TmaParams &p, const Tile &tl) { return Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0; }
 
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                 for (int kb = 0; kb < nk; ++kb) dev::tma_prefetch_3d(&p.tm_dv, tl.c0, kb * Cfg::KB, tl.n);
             }
             dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
-            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(tl), du_y<Cfg>(p, tl), tl.n, du_full);
+            dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(p, tl), du_y<Cfg>(p, tl), tl.n, du_full);
             du_issued = 1;
         }
         dev::grid_dependency_wait();
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                     break;
                 }
                 dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
-                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(tl), du_y<Cfg>(p, tl), tl.n, du_full);
+                dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(p, tl), du_y<Cfg>(p, tl), tl.n, du_full);
                 ++du_issued;
             }
         }
@@ -454,10 +456,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
     dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
     if (threadIdx.x == 0) trace_at(p, 1);
     // element-load offset configurations: the wide boxes hold the tile from float off on; shifted-grid ones: the
-    // d_u box starts 4 floats before the tile's box coordinate, and the tile's columns off_u - off_v after that
+    // tile's columns start off_u - off_v floats into the d_u box (4 more when the box starts 4 floats early)
     const int ox = Cfg::ELEM ? p.off_x : 0, ov = Cfg::ELEM ? p.off_v : 0;
+    const int su = p.off_u - p.off_v;
     const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) +
-                            (Cfg::ELEM ? p.off_u : (Cfg::SHIFT ? 4 + p.off_u - p.off_v : 0));
+                            (Cfg::ELEM ? p.off_u : (Cfg::SHIFT ? (su < 0 ? su + 4 : su) : 0));
     int it = 0;
     int tk = 0;
     for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x), ++tk) {
@@ -1231,15 +1234,16 @@ using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
 //   * the shifted grid (SHIFT_ = true): tiles are cut on the aligned-down maps' own grid, so tile (ib, cb) holds output
 //     rows ib TI - off_x .. and columns cb TC - off_v .., x and d_dv boxes are the tile's own size and the chain is the
 //     aligned kernel's, vector loads included; a step has ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles per
-//     chunk (rows and columns outside the operands are computed on zeros and not stored). The d_u box is 8 floats
-//     wider, from 4 floats before the tile's column coordinate, which covers the tile's columns for any off_u.
+//     chunk (rows and columns outside the operands are computed on zeros and not stored). The d_u box is 4 floats
+//     wider, from the tile's column coordinate (off_u >= off_v) or 4 floats before it (off_u < off_v), which covers
+//     the tile's columns for any off_u.
 // With every offset 0 either is the tile kernel on a few idle columns.
 template <class T, int EFF_, bool SHIFT_>
 struct OCfg : T {
     static constexpr int EFF = EFF_;
     static constexpr bool ELEM = !SHIFT_, SHIFT = SHIFT_;
     static constexpr int XP = SHIFT_ ? T::TI : T::TI + 4, DP = SHIFT_ ? T::TC : T::TC + 4;
-    static constexpr int UP = SHIFT_ ? T::TC + 8 : T::TC + 4;
+    static constexpr int UP = T::TC + 4;
     static constexpr int XS_BYTES = align_up(T::KB * XP * 4, 128);
     static constexpr int DS_BYTES = align_up(T::KB * DP * 4, 128);
     static constexpr int DU_BYTES = align_up(T::TI * UP * 4, 128);

@@ -177,8 +177,9 @@ OFFSET_PATTERNS = [(1, 1, 1), (2, 0, 3), (3, 2, 1), (0, 1, 0), (0, 0, 2)]   # fl
 @pytest.mark.parametrize("shape", [(3, 100, 76), (2, 48, 128), (5, 12, 4)])
 def test_offset_bases_every_offset_config(shape, offs):
     """Operand bases 4, 8 or 12 bytes past a 16-byte boundary, each operand its own offset: the plan takes an offset
-    configuration (TMA from aligned-down maps, boxes 4 floats wider), and every offset configuration, forced, gives the
-    oracle's bits, ragged in rows, columns and j, without touching the floats around the operands."""
+    configuration (TMA from aligned-down maps; element loads of wider boxes, or tiles on the shifted grid), and every
+    offset configuration, forced, gives the oracle's bits, ragged in rows, columns and j, without touching the floats
+    around the operands. A configuration of the aligned kernels, forced on such bases, is refused."""
     P, C, hd = shape
     w = synth.Workload("offset", 69, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
@@ -795,10 +796,10 @@ def test_latency_rule_prefers_small_tiles(shape):
 
 @pytest.mark.parametrize("layout", ["ld129", "offset4"])
 def test_generic_large_tile_kernel(layout):
-    """The generic path's large-tile kernel (128 x 64 tiles, packed FMAs, register-prefetched double-buffered staging)
-    on layouts TMA cannot describe: rows of 129 floats, and bases 4 bytes past a 16-byte boundary. 80 chunks of
-    C = 130, hd = 100 span several tiles per CTA with ragged rows, columns and j; the plan picks the kernel itself
-    once its tiles fill the SMs (here forced, then checked on a filling step)."""
+    """The generic path's large-tile kernel (128 x 64 tiles, packed FMAs, double-buffered cp.async staging) on layouts
+    TMA cannot describe: rows of 129 floats, and bases 4 bytes past a 16-byte boundary with x rows of 130 floats.
+    80 chunks of C = 130, hd = 100 span several tiles per CTA with ragged rows, columns and j; the plan picks the
+    kernel itself once its tiles fill the SMs (here forced, then checked on a filling step)."""
     w = synth.Workload("generic_big", 63, T=2, P=80, C=130, hd=100, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, w.P, range(w.T))
