@@ -35,6 +35,13 @@ def test_large_step_takes_the_stream_kernel_with_a_workspace():
     assert info(k0)["kind"] == "tile" and (info(k0)["TI"], info(k0)["TC"], info(k0)["consumer_warps"]) == (128, 128, 16)
 
 
+def test_many_tiles_per_sm_take_whole_tiles():
+    """Past 16 tiles a CTA the stream kernel is not offered: whole tiles then leave at most a sixteenth of a round idle
+    (8192 chunks of the large shape, 54 tiles an SM: 17.9 us a chunk-step on whole tiles against 18.4 split)."""
+    assert info(pick(8192, 128, 128))["kind"] == "tile"
+    assert info(pick(2048, 128, 128))["kind"] == "stream"   # 13.5 tiles an SM
+
+
 @pytest.mark.parametrize("shape,tile", [((32, 64, 128), (32, 64)),    # pdl_chain: 128 tiles of 32 x 64
                                         ((8, 64, 64), (8, 32)),       # producer_chain: 128 tiles of 8 x 32
                                         ((2, 16, 32), (8, 32)),       # tiny
