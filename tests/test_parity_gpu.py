@@ -411,8 +411,8 @@ def test_informative_cublas_cross_check():
     """The pages' second reference: cuBLAS FP32 batched GEMM (torch.baddbmm on the x.transpose(1, 2) view, TF32 off)
     computed the same chain on the configurations the page tested, but that is not a cuBLAS guarantee. Informative,
     as the page's qualification probe is set up: the six value patterns against every 4-byte base offset mod 256 of
-    each operand (the others 256-byte aligned; 16-byte-aligned offsets take the TMA kernels, the others the generic
-    one), and the bitwise agreement printed per pattern and operand. Required: finite results of both within the
+    each operand (the others 256-byte aligned; 16-byte-aligned offsets take the aligned TMA configurations, the others
+    the offset ones), and the bitwise agreement printed per pattern and operand. Required: finite results of both within the
     recursive-summation error bound of each other, and NaN from both wherever IEEE forces it in every order."""
     P, C, hd = 3, 64, 96
     bound_k = 2 * (C + 1) * 2.0 ** -24
