@@ -285,7 +285,8 @@ def kernel_name(gx, geom: dict) -> str:
     """The CUDA kernel a plan of this geometry launches per step."""
     if geom["path"] != 1:
         return "gx_generic_kernel"
-    return {"tile": "gx_tma_kernel", "offset": "gx_tma_kernel", "slab": "gx_slab_kernel", "stream": "gx_stream_kernel"}[
+    return {"tile": "gx_tma_kernel", "offset": "gx_tma_kernel", "offset_shifted": "gx_tma_kernel",
+            "slab": "gx_slab_kernel", "stream": "gx_stream_kernel"}[
         gx.config_info(1, geom["config"])["kind"]]
 
 

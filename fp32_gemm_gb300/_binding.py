@@ -429,11 +429,12 @@ def kernel_attrs(path: int, config: int) -> dict:
     return {"regs": out[0], "local_bytes": out[1], "static_smem": out[2], "max_threads": out[3]}
 
 
-CONFIG_KINDS = {0: "tile", 1: "slab", 2: "stream", 3: "offset"}
+CONFIG_KINDS = {0: "tile", 1: "slab", 2: "stream", 3: "offset", 4: "offset_shifted"}
 
 
 def config_info(path: int, config: int) -> dict:
-    """sdm_gx_gemm_config_info: the static description of a configuration (kind: tile / slab / stream)."""
+    """sdm_gx_gemm_config_info: the static description of a configuration (kind: tile / slab / stream / offset /
+    offset_shifted)."""
     out = (ctypes.c_int32 * 8)()
     _check(_lib.sdm_gx_gemm_config_info(int(path), int(config), out), "sdm_gx_gemm_config_info")
     return {"TI": out[0], "TC": out[1], "KB": out[2], "stages": out[3], "threads": out[4], "smem": out[5],

@@ -327,9 +327,9 @@ int stream_ctas_of(const DevState &d, int k) { return d.sms * std::max(0, d.tma_
 // static workspace of sdm_gx_gemm_step_noalloc, whose per-CTA launch counters stay equal only if every launch on it
 // counts the same CTAs).
 // offset: some operand base lies off a 16-byte boundary; only the offset configurations (kind 3) serve it, and only
-// it takes them unless forced.
+// it takes them unless forced; shift_ok: d_u and d_dv lie equally far off (the shifted-grid ones need that).
 int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int forced, size_t ws_bytes,
-                      int stream_ctas_only, bool offset = false) {
+                      int stream_ctas_only, bool offset = false, bool shift_ok = true) {
     if (forced >= 0) return forced;
     auto tiles_of = [&](const ConfigInfo &ci) {
         const int64_t g = ci.kind == 3 && ci.shifted ? 3 : 0;   // the shifted grid's extra rows and columns, at most
@@ -337,7 +337,7 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     };
     auto usable = [&](int k) {
         const ConfigInfo &ci = tma_config(k);
-        return d.tma_occ[k] >= 1 && (ci.kind == 3) == offset &&
+        return d.tma_occ[k] >= 1 && (ci.kind == 3) == offset && (shift_ok || !(ci.kind == 3 && ci.shifted)) &&
                config_eligible(ci, P, C, hd, stream_ctas_of(d, k), ws_bytes) &&
                !(ci.kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) &&
                !(ci.kind == 1 && !d.slab_ok) && tiles_of(ci) < kTwo31;
@@ -347,10 +347,12 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     // parallel chains of the least work each. Among equally many tiles the smaller tile wins (a CTA's time follows
     // its tile's area, rows and columns past C and hd included: 128 x 64 tiles on C = 64 took 5.8 us a step where
     // 64 x 64 tiles took 4.2), then the more efficient configuration.
+    // (A property of the step's shape, judged on the aligned tile kernels whatever the layout: the offset menu has no
+    // tile of 32+ outputs per thread small enough to tell.)
     bool throughput = false;
     for (int k = 0; k < tma_num_configs(); ++k) {
         const ConfigInfo &ci = tma_config(k);
-        if (usable(k) && ci.RM * ci.RN >= 32 && tiles_of(ci) >= d.sms) throughput = true;
+        if (ci.kind == 0 && d.tma_occ[k] >= 1 && ci.RM * ci.RN >= 32 && tiles_of(ci) >= d.sms) throughput = true;
     }
     if (!throughput) {
         int bk = -1;
@@ -459,11 +461,12 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
     int occ = 0;
     if (use_tma) {
         if (forced >= tma_num_configs()) return SDM_GX_E_FLAGS;
-        const int k =
-            choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, stream_ctas_only, offs);
+        const bool shift_ok = floats_off(du0) == floats_off(dv0);
+        const int k = choose_tma_config(d, sh.P, sh.C, sh.hd, forced, ws != nullptr ? ws_bytes : 0, stream_ctas_only,
+                                        offs, shift_ok);
         if (k < 0) return SDM_GX_E_SMEM;
         ci = &tma_config(k);
-        if ((offs && ci->kind != 3) ||
+        if ((offs && ci->kind != 3) || (ci->kind == 3 && ci->shifted && !shift_ok) ||
             !config_eligible(*ci, sh.P, sh.C, sh.hd, stream_ctas_of(d, k), ws != nullptr ? ws_bytes : 0) ||
             (ci->kind == 2 && stream_ctas_only > 0 && stream_ctas_of(d, k) != stream_ctas_only) ||
             (ci->kind == 1 && !d.slab_ok))
@@ -478,10 +481,10 @@ int build_launch(float *du, const float *x, const float *dv, const Shape &sh, in
         const int du_rows = ci->kind == 1 ? 4 * ci->TI : ci->TI;   // slab kernel: a full round is four slabs
         // offset configurations: each map from its base rounded down to 16 bytes, the innermost extent grown by the
         // offset; element-load ones take boxes 4 floats wider (the tile from float off of each box row on), shifted-
-        // grid ones the tile's own x and d_dv boxes and a d_u box 4 floats wider
+        // grid ones the tile's own boxes (off_u == off_v)
         const bool k3 = ci->kind == 3, shifted = k3 && ci->shifted;
         const int ox = k3 ? floats_off(x0) : 0, ov = k3 ? floats_off(dv0) : 0, ou = k3 ? floats_off(du0) : 0;
-        const int wide = k3 && !shifted ? 4 : 0, wide_u = k3 ? 4 : 0;
+        const int wide = k3 && !shifted ? 4 : 0, wide_u = wide;
         t.off_x = ox;
         t.off_v = ov;
         t.off_u = ou;
@@ -1267,7 +1270,7 @@ int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]) {
     out[3] = ci->stages;
     out[4] = ci->threads;
     out[5] = ci->smem;
-    out[6] = path == 1 ? ci->kind : 0;
+    out[6] = path == 1 ? (ci->kind == 3 && ci->shifted ? 4 : ci->kind) : 0;
     out[7] = ci->consumer_warps;
     return SDM_GX_OK;
 }

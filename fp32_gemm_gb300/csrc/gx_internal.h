@@ -75,7 +75,7 @@ struct ConfigInfo {
                 // 2: stream kernel (the step's (tile, j) work split evenly over the CTAs; needs a plan workspace);
                 // 3: tile kernel for operand bases off a 16-byte boundary (aligned-down tensor maps)
     int shifted;   // kind 3: 0 element loads of boxes 4 floats wider; 1 tiles on the shifted grid
-                   // (ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles a chunk, a d_u box 4 floats wider)
+                   // (ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles a chunk; needs off_u == off_v)
 };
 
 // Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,

@@ -204,16 +204,16 @@ __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const 
 }
 
 // Epilogue: d_u + acc with one rounding each (the staged d_u tile us[TI][TC]), stored straight to global memory with
-// vector stores; a vector that straddles hd, or one whose d_u address is off a 16-byte boundary (offset
+// vector stores; a vector that straddles hd, or one whose d_u address is off a 16-byte boundary (element-load offset
 // configurations), is stored element by element; rows outside 0..C-1 and columns outside 0..hd-1 are skipped.
-// Shifted-grid configurations: the tile's output rows and columns start off_x and off_v before its box coordinates,
-// and us points at the tile's first column inside the wider d_u box (vector reads when off_u == off_v).
+// Shifted-grid configurations: the tile's output rows and columns start off_x and off_v (= off_u) before its box
+// coordinates; its d_u vectors then sit on 16-byte boundaries again.
 template <class Cfg>
 __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, const float *us, const int (&ro)[Cfg::SR],
                                          const int (&co)[Cfg::SN], const float (&acc)[Cfg::RM][Cfg::RN]) {
     const int ir0 = Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0;
     const int cr0 = Cfg::SHIFT ? tl.c0 - p.off_v : tl.c0;
-    const bool vec = !Cfg::ELEM && (!Cfg::SHIFT || p.off_u == p.off_v);
+    constexpr bool vec = !Cfg::ELEM;
 #pragma unroll
     for (int sr = 0; sr < Cfg::SR; ++sr) {
 #pragma unroll
@@ -228,7 +228,7 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
                 const int c = cr0 + cl;
                 if (c >= p.hd || (Cfg::SHIFT && c + Cfg::VN <= 0)) continue;
                 float u[Cfg::VN], o[Cfg::VN];
-                if (vec) {
+                if constexpr (vec) {
                     dev::Vec<Cfg::VN>::load(us + rl * Cfg::UP + cl, u);
                 } else {
 #pragma unroll
@@ -322,12 +322,10 @@ __device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl
 }
 
 // Coordinates of a tile's d_u box: the tile's own, or on the shifted grid off_x rows before its row coordinate (the
-// tile's first output row) and, when off_u < off_v, 4 floats before its column coordinate (an aligned x; the box is 4
-// floats wider than the tile); a negative row or column coordinate reads zeros.
+// tile's first output row; a negative row coordinate reads zeros). The column coordinate is the tile's own: the
+// shifted grid requires off_u == off_v, so the box's columns are the tile's.
 template <class Cfg>
-__device__ __forceinline__ int du_x(const TmaParams &p, const Tile &tl) {
-    return Cfg::SHIFT && p.off_u < p.off_v ? tl.c0 - 4 : tl.c0;
-}
+__device__ __forceinline__ int du_x(const TmaParams &, const Tile &tl) { return tl.c0; }
 template <class Cfg>
 __device__ __forceinline__ int du_y(const TmaParams &p, const Tile &tl) { return Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0; }
 
@@ -455,12 +453,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
 
     dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
     if (threadIdx.x == 0) trace_at(p, 1);
-    // element-load offset configurations: the wide boxes hold the tile from float off on; shifted-grid ones: the
-    // tile's columns start off_u - off_v floats into the d_u box (4 more when the box starts 4 floats early)
+    // element-load offset configurations: the wide boxes hold the tile from float off on
     const int ox = Cfg::ELEM ? p.off_x : 0, ov = Cfg::ELEM ? p.off_v : 0;
-    const int su = p.off_u - p.off_v;
-    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) +
-                            (Cfg::ELEM ? p.off_u : (Cfg::SHIFT ? (su < 0 ? su + 4 : su) : 0));
+    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) + (Cfg::ELEM ? p.off_u : 0);
     int it = 0;
     int tk = 0;
     for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x), ++tk) {
@@ -1234,16 +1229,17 @@ using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
 //   * the shifted grid (SHIFT_ = true): tiles are cut on the aligned-down maps' own grid, so tile (ib, cb) holds output
 //     rows ib TI - off_x .. and columns cb TC - off_v .., x and d_dv boxes are the tile's own size and the chain is the
 //     aligned kernel's, vector loads included; a step has ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles per
-//     chunk (rows and columns outside the operands are computed on zeros and not stored). The d_u box is 4 floats
-//     wider, from the tile's column coordinate (off_u >= off_v) or 4 floats before it (off_u < off_v), which covers
-//     the tile's columns for any off_u.
+//     chunk (rows and columns outside the operands are computed on zeros and not stored). It needs off_u == off_v:
+//     the d_u box is then the tile's own size at the tile's column coordinate, and the epilogue's vectors are aligned.
+//     (A d_u box wider than the tile, covering any off_u, measured 12% slower on small steps whenever a box ran past
+//     the operand's columns.)
 // With every offset 0 either is the tile kernel on a few idle columns.
 template <class T, int EFF_, bool SHIFT_>
 struct OCfg : T {
     static constexpr int EFF = EFF_;
     static constexpr bool ELEM = !SHIFT_, SHIFT = SHIFT_;
     static constexpr int XP = SHIFT_ ? T::TI : T::TI + 4, DP = SHIFT_ ? T::TC : T::TC + 4;
-    static constexpr int UP = T::TC + 4;
+    static constexpr int UP = SHIFT_ ? T::TC : T::TC + 4;
     static constexpr int XS_BYTES = align_up(T::KB * XP * 4, 128);
     static constexpr int DS_BYTES = align_up(T::KB * DP * 4, 128);
     static constexpr int DU_BYTES = align_up(T::TI * UP * 4, 128);

@@ -167,7 +167,7 @@ def test_edge_patterns(vset, variant):
 
 
 def _offset_configs():
-    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "offset"]
+    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"].startswith("offset")]
 
 
 OFFSET_PATTERNS = [(1, 1, 1), (2, 0, 3), (3, 2, 1), (0, 1, 0), (0, 0, 2)]   # floats past 16 bytes: d_u, x, d_dv
@@ -179,7 +179,8 @@ def test_offset_bases_every_offset_config(shape, offs):
     """Operand bases 4, 8 or 12 bytes past a 16-byte boundary, each operand its own offset: the plan takes an offset
     configuration (TMA from aligned-down maps; element loads of wider boxes, or tiles on the shifted grid), and every
     offset configuration, forced, gives the oracle's bits, ragged in rows, columns and j, without touching the floats
-    around the operands. A configuration of the aligned kernels, forced on such bases, is refused."""
+    around the operands. A configuration of the aligned kernels, forced on such bases, is refused, and so is a
+    shifted-grid one where d_u and d_dv lie differently far off."""
     P, C, hd = shape
     w = synth.Workload("offset", 69, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
@@ -190,9 +191,14 @@ def test_offset_bases_every_offset_config(shape, offs):
     for k in [None] + cfgs:
         du = DevArray(inp["d_u"], offs[0])
         dx, dv = DevArray(inp["x"], offs[1]), DevArray(inp["d_dv"], offs[2])
+        if k is not None and gx.config_info(1, k)["kind"] == "offset_shifted" and offs[0] != offs[2]:
+            with pytest.raises(gx.GxGemmError) as e:   # the shifted grid needs d_u and d_dv equally far off
+                gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+            assert e.value.name == "SDM_GX_E_FLAGS"
+            continue
         pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=0 if k is None else gx.config_flag(k))
         g = pl.geometry()
-        assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"] == "offset", g
+        assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"].startswith("offset"), g
         if k is None:
             auto = g["config"]
         pl.run(1, -1, pdl=True)
@@ -217,7 +223,7 @@ def test_offset_bases_large_shape():
     du, dx, dv = _dev(inp, offset=1)
     pl = gx.Plan(du.t, dx.t, dv.t, w.P)
     g = pl.geometry()
-    assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"] == "offset", g
+    assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"].startswith("offset"), g
     pl.run(pdl=True)
     torch.cuda.synchronize()
     assert_bitwise(du.host(), want, "large 2 steps, offset bases")
