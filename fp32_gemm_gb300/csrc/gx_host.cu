@@ -347,7 +347,7 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
     // parallel chains of the least work each. Among equally many tiles the smaller tile wins (a CTA's time follows
     // its tile's area, rows and columns past C and hd included: 128 x 64 tiles on C = 64 took 5.8 us a step where
     // 64 x 64 tiles took 4.2), then the more efficient configuration.
-    // (A property of the step's shape, judged on the aligned tile kernels whatever the layout: the offset menu has no
+    // (A property of the step's shape, decided on the aligned tile kernels whatever the layout: the offset menu has no
     // tile of 32+ outputs per thread small enough to tell.)
     bool throughput = false;
     for (int k = 0; k < tma_num_configs(); ++k) {
