@@ -73,6 +73,28 @@ def test_noalloc_interleaved_shapes():
             assert_bitwise(got[n], want[n], f"interleaved P={P} chunk {n}")
 
 
+def test_noalloc_offset_bases():
+    """Operands 4 bytes past a 16-byte boundary (contiguous views at a storage offset of one float): the allocation-free
+    call takes the TMA path's offset configurations like the stateless call, with the same bits."""
+    from tests.gpu_util import DevArray
+    inp, _ = _inputs(32, 64, 128)
+    ref = [DevArray(inp[k], 1) for k in ("d_u", "x", "d_dv")]
+    new = [DevArray(inp[k], 1) for k in ("d_u", "x", "d_dv")]
+    g = gx.noalloc_geometry(new[0].t, new[1].t, new[2].t, 32)
+    assert g["path"] == 1 and gx.config_info(1, g["config"])["kind"].startswith("offset"), g
+    gx.device_error(clear=True)
+    for ti in (1, 0):
+        gx.step(ref[0].t, ref[1].t, ref[2].t, ti, 32, pdl=True)
+        gx.step_noalloc(new[0].t, new[1].t, new[2].t, ti, 32, pdl=True)
+    torch.cuda.synchronize()
+    assert gx.device_error(clear=True) == 0
+    assert_bitwise(new[0].host(), ref[0].host(), "noalloc vs step, offset bases")
+    want = inp["d_u"].copy()
+    oracle.run_steps(want, inp["x"], inp["d_dv"], 32, order=[1, 0])
+    assert_bitwise(new[0].host(), want, "noalloc offset bases vs oracle")
+    assert all(a.guards_intact() for a in new)
+
+
 def test_noalloc_rejects_what_step_rejects():
     t = torch.zeros(4, 8, 8, device="cuda")
     with pytest.raises(gx.GxGemmError) as e:
