@@ -246,7 +246,7 @@ constexpr double kMemBytesPerUs = 7.0e6;
 // fitted FMA rate per SM, as a fraction of 128 lanes a cycle, by configuration (the order of the TMA configuration
 // table); a configuration past the table falls back to its kernel's own efficiency figure
 constexpr double kRate[] = {0.797, 0.747, 0.749, 0.752, 0.763, 0.721, 0.709, 0.677, 0.433, 0.430, 0.365,
-                            0.731, 1.000, 0.971, 0.940, 0.565, 0.480, 0.630, 0.305};
+                            0.731, 1.000, 0.971, 0.940, 0.590, 0.480, 0.630, 0.305};
 constexpr int kRates = static_cast<int>(sizeof(kRate) / sizeof(kRate[0]));
 }  // namespace model
 

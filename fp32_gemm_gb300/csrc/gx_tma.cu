@@ -39,6 +39,8 @@ struct TCfg {
     static constexpr bool DUPRE = false;           // stream kernel only: d_u read into registers in the last stage
     static constexpr bool ELEM = false;            // offset configurations (OCfg): element loads of wide boxes
     static constexpr bool SHIFT = false;           // offset configurations (OCfg): tiles on the shifted grid
+    static constexpr bool REALIGN = false;         // offset configurations (OCfg): wide boxes realigned per stage
+    static constexpr bool UELEM = false;           // the staged d_u box is read, and d_u stored, element by element
     static constexpr int RM = RM_, RN = RN_;       // per-thread tile: rows x columns
     static constexpr int WM = WM_, WN = WN_;       // consumer warps along rows / columns
     static constexpr int KB = KB_, ST = ST_;       // j rows per stage, stages
@@ -213,7 +215,7 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
                                          const int (&co)[Cfg::SN], const float (&acc)[Cfg::RM][Cfg::RN]) {
     const int ir0 = Cfg::SHIFT ? tl.i0 - p.off_x : tl.i0;
     const int cr0 = Cfg::SHIFT ? tl.c0 - p.off_v : tl.c0;
-    constexpr bool vec = !Cfg::ELEM;
+    constexpr bool vec = !Cfg::UELEM;
 #pragma unroll
     for (int sr = 0; sr < Cfg::SR; ++sr) {
 #pragma unroll
@@ -321,6 +323,73 @@ __device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl
     }
 }
 
+// Realigning offset configurations: warp w shifts rows w, w + NCW, .. of the stage's x box [KB][TI + 4] (then of its
+// d_dv box [KB][TC + 4]) left by the operand's offset (0..3 floats) into the aligned buffers xa [KB][TI], da [KB][TC].
+// A row is one warp-wide pass: lane l reads the box row's 16-byte vector l, takes the next one from lane l + 1 (lane
+// 31 reads vector 32, the box's extra 4 floats), and writes aligned vector l from the two.
+template <int OFF>
+__device__ __forceinline__ float4 shift_left(float4 a, float4 b) {
+    if constexpr (OFF == 0) return a;
+    if constexpr (OFF == 1) return make_float4(a.y, a.z, a.w, b.x);
+    if constexpr (OFF == 2) return make_float4(a.z, a.w, b.x, b.y);
+    return make_float4(a.w, b.x, b.y, b.z);
+}
+
+template <int W>
+__device__ __forceinline__ void realign_rows(const float *raw, float *al, int rows, int off, int warp, int nwarps,
+                                             int lane) {
+    static_assert(W == 128, "a box row is one warp-wide pass of 16-byte vectors");
+    for (int r = warp; r < rows; r += nwarps) {
+        const float4 *src = reinterpret_cast<const float4 *>(raw + r * (W + 4));
+        const float4 a = src[lane];
+        float4 b;
+        b.x = __shfl_down_sync(0xffffffffu, a.x, 1);
+        b.y = __shfl_down_sync(0xffffffffu, a.y, 1);
+        b.z = __shfl_down_sync(0xffffffffu, a.z, 1);
+        b.w = __shfl_down_sync(0xffffffffu, a.w, 1);
+        if (lane == 31) b = src[32];
+        float4 o;
+        switch (off) {
+            case 0: o = shift_left<0>(a, b); break;
+            case 1: o = shift_left<1>(a, b); break;
+            case 2: o = shift_left<2>(a, b); break;
+            default: o = shift_left<3>(a, b); break;
+        }
+        reinterpret_cast<float4 *>(al + r * W)[lane] = o;
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void realign_stage(const float *xr, const float *dr, float *xa, float *da, int off_x,
+                                              int off_v, int warp, int lane) {
+    realign_rows<Cfg::TI>(xr, xa, Cfg::KB, off_x, warp, Cfg::NCW, lane);
+    realign_rows<Cfg::TC>(dr, da, Cfg::KB, off_v, (warp + Cfg::KB) % Cfg::NCW, Cfg::NCW, lane);
+}
+
+// Realigning configurations: stage iteration k's staged boxes (raw stage k % ST) into aligned buffer k % 3; then the
+// raw stage is released to the producer and buffer k % 3 marked with this warp's arrival. False: the staged boxes never
+// came (the device error word is set).
+template <class Cfg>
+__device__ __forceinline__ bool realign_ahead(const TmaParams &p, unsigned char *base_g, uint32_t bar0,
+                                              uint32_t du_empty, int k, int warp, int lane) {
+    const int s = k % Cfg::ST;
+    if (!__all_sync(0xffffffffu,
+                    dev::mbar_wait(bar0 + 8u * s, static_cast<uint32_t>(k / Cfg::ST) & 1u, p.timeout_ns))) {
+        if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+        return false;
+    }
+    const float *xr = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
+    const float *dr = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
+    float *xa = reinterpret_cast<float *>(base_g + Cfg::OFF_A + (k % 3) * Cfg::A_BYTES);
+    realign_stage<Cfg>(xr, dr, xa, xa + Cfg::KB * Cfg::TI, p.off_x, p.off_v, warp, lane);
+    __syncwarp();
+    if (lane == 0) {
+        dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+        dev::mbar_arrive(du_empty + 8u + 8u * static_cast<uint32_t>(k % 3));
+    }
+    return true;
+}
+
 // Coordinates of a tile's d_u box: the tile's own, or on the shifted grid off_x rows before its row coordinate (the
 // tile's first output row; a negative row coordinate reads zeros). The column coordinate is the tile's own: the
 // shifted grid requires off_u == off_v, so the box's columns are the tile's.
@@ -348,6 +417,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
         }
         dev::mbar_init(du_full, 1);
         dev::mbar_init(du_empty, Cfg::NCW);
+        if constexpr (Cfg::REALIGN) {   // realigned[b]: every consumer warp has realigned its rows into buffer b
+            for (int bsel = 0; bsel < 3; ++bsel) dev::mbar_init(du_empty + 8u + 8u * bsel, Cfg::NCW);
+        }
         dev::fence_mbar_init();
     }
     __syncthreads();
@@ -453,9 +525,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
 
     dev::grid_dependency_wait();   // d_u is written below only after the predecessor grid has completed
     if (threadIdx.x == 0) trace_at(p, 1);
-    // element-load offset configurations: the wide boxes hold the tile from float off on
+    // element-load offset configurations: the wide boxes hold the tile from float off on (and the d_u box of the
+    // realigning ones too)
     const int ox = Cfg::ELEM ? p.off_x : 0, ov = Cfg::ELEM ? p.off_v : 0;
-    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) + (Cfg::ELEM ? p.off_u : 0);
+    const float *const us = reinterpret_cast<const float *>(base_g + Cfg::OFF_U) + (Cfg::UELEM ? p.off_u : 0);
+    // stage iterations of this CTA (realigning configurations look one ahead)
+    const int it_total = static_cast<int>(blockIdx.x) < p.ntiles
+                             ? ((p.ntiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1) * nk
+                             : 0;
     int it = 0;
     int tk = 0;
     for (int t = static_cast<int>(blockIdx.x); t < p.ntiles; t += static_cast<int>(gridDim.x), ++tk) {
@@ -469,22 +546,40 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
         for (int kb = 0; kb < nk; ++kb, ++it) {
             const int s = it % Cfg::ST;
             const uint32_t ph = static_cast<uint32_t>(it / Cfg::ST) & 1u;
-            // warp-uniform decision: every lane leaves together or none does
-            if (!__all_sync(0xffffffffu, dev::mbar_wait(bar0 + 8u * s, ph, p.timeout_ns))) {
+            // warp-uniform decision: every lane leaves together or none does (realigning configurations wait for
+            // the staged boxes when they realign them)
+            if (!Cfg::REALIGN && !__all_sync(0xffffffffu, dev::mbar_wait(bar0 + 8u * s, ph, p.timeout_ns))) {
                 if (lane == 0) atomicOr(p.err, kErrConsumerWait);
                 return;
             }
 
             const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES) + ox;
             const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES) + ov;
+            if constexpr (Cfg::REALIGN) {
+                // Realigned one stage ahead: stage it is computed from buffer it % 3, whose rows every warp wrote
+                // during its previous iteration; once every warp's rows are there, this warp writes its rows of stage
+                // it + 1 into buffer (it + 1) % 3. That buffer last held stage it - 2, and every warp finished
+                // computing stage it - 2 before it realigned stage it (its arrival on buffer it % 3).
+                if (it == 0 && !realign_ahead<Cfg>(p, base_g, bar0, du_empty, 0, warp, lane)) return;
+                const uint32_t b = du_empty + 8u + 8u * static_cast<uint32_t>(it % 3);
+                if (!__all_sync(0xffffffffu, dev::mbar_wait(b, static_cast<uint32_t>(it / 3) & 1u, p.timeout_ns))) {
+                    if (lane == 0) atomicOr(p.err, kErrConsumerWait);
+                    return;
+                }
+                if (it + 1 < it_total && !realign_ahead<Cfg>(p, base_g, bar0, du_empty, it + 1, warp, lane)) return;
+                xs = reinterpret_cast<const float *>(base_g + Cfg::OFF_A + (it % 3) * Cfg::A_BYTES);
+                ds = xs + Cfg::KB * Cfg::TI;
+            }
             const int nj = p.C - kb * Cfg::KB;
             if (nj >= Cfg::KB) {
                 chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
             } else {
                 chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
             }
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+            if constexpr (!Cfg::REALIGN) {
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
+            }
         }
         if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(tk) & 1u, p.timeout_ns))) {
             if (lane == 0) atomicOr(p.err, kErrConsumerWait);
@@ -521,7 +616,7 @@ struct SCfg {
     static constexpr int TC = WN * RN * LN;        // 128 columns
     static constexpr int NCW = WS * WN;            // 16 consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;
-    static constexpr bool ELEM = false, SHIFT = false;
+    static constexpr bool ELEM = false, SHIFT = false, REALIGN = false, UELEM = false;
     static constexpr int XP = TI, DP = TC, UP = TC;
     static constexpr int X_SLAB = KB * TI * 4;     // bytes of one slab's x rows per stage
     static constexpr int D_BOX = KB * TC * 4;
@@ -1191,7 +1286,7 @@ const void *kernel_of() {
 template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF, (Cfg::ELEM || Cfg::SHIFT) ? 3 : Cfg::SLAB, Cfg::SHIFT ? 1 : 0};
+                      Cfg::EFF, (Cfg::ELEM || Cfg::SHIFT || Cfg::REALIGN) ? 3 : Cfg::SLAB, Cfg::SHIFT ? 1 : 0};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the
@@ -1221,40 +1316,49 @@ using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
 // strides that are multiples of 16 bytes: a slice at an odd offset, say). TMA needs 16-byte-aligned bases and innermost
 // coordinates, so the host encodes each operand's map from its base rounded down to 16 bytes, with the innermost
 // extent grown by the offset (off = 1..3 floats; the map's rows then overlap the previous row's last off floats, which
-// are loaded and never used). Two ways to use such maps:
-//   * element loads (SHIFT_ = false): every box is 4 floats wider than the tile, so that a box at the tile's own
+// are loaded and never used). Three ways to use such maps:
+//   * element loads (MODE_ = 0): every box is 4 floats wider than the tile, so that a box at the tile's own
 //     (aligned) coordinate holds the tile's columns from float off on; the consumers read the staged boxes at that
 //     offset with element loads (vectors would straddle 16-byte boundaries) and store d_u element by element. The
 //     tiles are the aligned kernel's; the chain's shared loads are four times as many.
-//   * the shifted grid (SHIFT_ = true): tiles are cut on the aligned-down maps' own grid, so tile (ib, cb) holds output
+//   * the shifted grid (MODE_ = 1): tiles are cut on the aligned-down maps' own grid, so tile (ib, cb) holds output
 //     rows ib TI - off_x .. and columns cb TC - off_v .., x and d_dv boxes are the tile's own size and the chain is the
 //     aligned kernel's, vector loads included; a step has ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles per
 //     chunk (rows and columns outside the operands are computed on zeros and not stored). It needs off_u == off_v:
 //     the d_u box is then the tile's own size at the tile's column coordinate, and the epilogue's vectors are aligned.
 //     (A d_u box wider than the tile, covering any off_u, measured 12% slower on small steps whenever a box ran past
 //     the operand's columns.)
-// With every offset 0 either is the tile kernel on a few idle columns.
-template <class T, int EFF_, bool SHIFT_>
+//   * realigned stages (MODE_ = 2): the element-load layout's wide boxes, which the consumer warps shift onto 16-byte
+//     boundaries one stage ahead into three aligned buffers (each warp a share of the rows, then an mbarrier that every
+//     consumer warp arrives on), so that the chain runs the aligned kernel's vector loads; a tenth more shared-memory
+//     traffic instead of four times the load instructions.
+// With every offset 0 each is the tile kernel on a few idle columns.
+template <class T, int EFF_, int MODE_>   // MODE_: 0 element loads, 1 shifted grid, 2 realigned stages
 struct OCfg : T {
     static constexpr int EFF = EFF_;
-    static constexpr bool ELEM = !SHIFT_, SHIFT = SHIFT_;
-    static constexpr int XP = SHIFT_ ? T::TI : T::TI + 4, DP = SHIFT_ ? T::TC : T::TC + 4;
-    static constexpr int UP = SHIFT_ ? T::TC : T::TC + 4;
-    static constexpr int XS_BYTES = align_up(T::KB * XP * 4, 128);
-    static constexpr int DS_BYTES = align_up(T::KB * DP * 4, 128);
+    static constexpr bool ELEM = MODE_ == 0, SHIFT = MODE_ == 1, REALIGN = MODE_ == 2, UELEM = MODE_ != 1;
+    static constexpr int RX = SHIFT ? T::TI : T::TI + 4, RD = SHIFT ? T::TC : T::TC + 4;   // staged box row pitches
+    static constexpr int XP = ELEM ? RX : T::TI, DP = ELEM ? RD : T::TC;   // the pitches the chain reads with
+    static constexpr int UP = SHIFT ? T::TC : T::TC + 4;
+    static constexpr int XS_BYTES = align_up(T::KB * RX * 4, 128);
+    static constexpr int DS_BYTES = align_up(T::KB * RD * 4, 128);
     static constexpr int DU_BYTES = align_up(T::TI * UP * 4, 128);
+    static constexpr int A_BYTES = REALIGN ? T::KB * (T::TI + T::TC) * 4 : 0;   // one aligned buffer: x, then d_dv
     static constexpr int OFF_D = T::ST * XS_BYTES;
     static constexpr int OFF_U = OFF_D + T::ST * DS_BYTES;
-    static constexpr int OFF_BAR = OFF_U + DU_BYTES;
-    static constexpr int SMEM = OFF_BAR + align_up(T::NBAR * 8, 128) + 128;
-    static constexpr uint32_t STAGE_TX = static_cast<uint32_t>(T::KB * (XP + DP) * 4);
+    static constexpr int OFF_A = OFF_U + DU_BYTES;
+    static constexpr int OFF_BAR = OFF_A + 3 * A_BYTES;
+    static constexpr int NBAR = T::NBAR + (REALIGN ? 3 : 0);
+    static constexpr int SMEM = OFF_BAR + align_up(NBAR * 8, 128) + 128;
+    static constexpr uint32_t STAGE_TX = static_cast<uint32_t>(T::KB * (RX + RD) * 4);
     static constexpr uint32_t DU_TX = static_cast<uint32_t>(T::TI * UP * 4);
-    static_assert(XP <= 256 && DP <= 256, "TMA box dimensions are at most 256");
+    static_assert(RX <= 256 && RD <= 256, "TMA box dimensions are at most 256");
+    static_assert(!REALIGN || (T::TI == 128 && T::TC == 128 && T::KB % 4 == 0), "realigned rows: one warp pass each");
 };
-using C15 = OCfg<C0, 60, false>;   // 128 x 128, 16 warps, element loads: steps that fill the SMs
-using C16 = OCfg<C7, 50, false>;   //  32 x  64, 4 warps, element loads
-using C17 = OCfg<C7, 60, true>;    //  32 x  64, 4 warps, shifted grid
-using C18 = OCfg<C10, 20, true>;   //   8 x  32, 1 warp, shifted grid: the smallest steps
+using C15 = OCfg<C0, 60, 2>;    // 128 x 128, 16 warps, realigned stages: steps that fill the SMs
+using C16 = OCfg<C7, 50, 0>;    //  32 x  64, 4 warps, element loads
+using C17 = OCfg<C7, 60, 1>;    //  32 x  64, 4 warps, shifted grid
+using C18 = OCfg<C10, 20, 1>;   //   8 x  32, 1 warp, shifted grid: the smallest steps
 
 struct Entry {
     ConfigInfo info;
