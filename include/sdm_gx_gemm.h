@@ -350,9 +350,9 @@ SDM_GX_API int sdm_gx_gemm_kernel_attrs(int32_t path, int32_t config, int64_t ou
 /* Static description of configuration `config` of a path (for sweeps and tests; the page's kernel has one tile width
  * TC = 64 and a row count chosen per launch by _rows, this library a menu of tiles): out[0..7] = TI, TC, KB, stages,
  * threads per CTA, dynamic shared memory bytes, kind (0: tile kernel, 1: balanced slab kernel, 2: stream kernel, which
- * needs a plan workspace, 3: tile kernel for bases off a 16-byte boundary with element loads of wider boxes, 4: the
- * same on the shifted tile grid, which needs d_u and d_dv equally far off), consumer warps. SDM_GX_E_FLAGS for an
- * unknown path or index. */
+ * needs a plan workspace, 3: tile kernel for bases off a 16-byte boundary, its boxes 4 floats wider and read by
+ * element loads or realigned once per stage, 4: the same on the shifted tile grid, which needs d_u and d_dv equally
+ * far off), consumer warps. SDM_GX_E_FLAGS for an unknown path or index. */
 SDM_GX_API int sdm_gx_gemm_config_info(int32_t path, int32_t config, int32_t out[8]);
 
 /* The stream kernel's split of a step (no counterpart on the pages, which give every chunk's tile to one CTA; the
