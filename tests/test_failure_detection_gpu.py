@@ -1,4 +1,4 @@
-"""Failure detection without a GPU fault: the test hook makes the TMA kernel's producer withhold its first stage, so
+"""Failure detection without a GPU fault: the test hook makes the TMA kernels' producer withhold its first stage, so
 every wait on it runs out after its short bound (~20 ms). The launch must complete, the device error word must report
 the expired waits, and the context must stay usable: a normal launch right after gives oracle-exact results."""
 
@@ -97,3 +97,30 @@ def test_stream_kernel_late_handoff_recomputes_exactly():
     oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
     assert_bitwise(du.host(), want, "normal launch after the late hand-offs")
     assert gx.device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("kind", ["offset", "offset_shifted"])
+def test_offset_configurations_expired_waits_are_reported(kind):
+    """The stall hook on the offset configurations (bases 4 bytes past a 16-byte boundary; the realigning 128 x 128
+    one waits on its aligned buffers too): every forced configuration of the kind completes its stalled launch with
+    the error word set, and a normal launch after it is oracle-exact."""
+    w = synth.Workload("stall_offset", 79, T=2, P=3, C=64, hd=128, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    cfgs = [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == kind]
+    assert cfgs
+    for k in cfgs:
+        du, dx, dv = (DevArray(inp[n], 1) for n in ("d_u", "x", "d_dv"))
+        gx.device_error(clear=True)
+        stalled = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.FLAG_TEST_STALL | gx.config_flag(k))
+        stalled.step(0)
+        torch.cuda.synchronize()
+        word = gx.device_error(clear=True)
+        assert word & 1, f"config {k}: consumer wait not reported: {word:#x}"
+        du2, dx2, dv2 = (DevArray(inp[n], 1) for n in ("d_u", "x", "d_dv"))
+        ok = gx.Plan(du2.t, dx2.t, dv2.t, w.P, flags=gx.config_flag(k))
+        ok.run(pdl=True)
+        torch.cuda.synchronize()
+        want = inp["d_u"].copy()
+        oracle.run_steps(want, inp["x"], inp["d_dv"], w.P)
+        assert_bitwise(du2.host(), want, f"config {k} after the stall test")
+        assert gx.device_error(clear=True) == 0
