@@ -107,3 +107,41 @@ def test_noalloc_geometry_flag_alone():
     with pytest.raises(gx.GxGemmError) as e:
         gx.geometry(dev["d_u"], dev["x"], dev["d_dv"], 8, flags=gx.FLAG_NOALLOC | gx.FLAG_GENERIC)
     assert e.value.name == "SDM_GX_E_FLAGS"
+
+
+_CAPTURE_CHILD = r"""
+import json, torch
+import fp32_gemm_gb300 as gx
+P, C, hd = 8, 64, 64
+x = torch.randn(2 * P, C, C, device="cuda") * 0.1
+dv = torch.randn(2 * P, C, hd, device="cuda")
+du = torch.randn(2 * P, C, hd, device="cuda")
+gx.geometry(du, x, dv, P)   # the library's per-device set-up happens outside the capture
+g = torch.cuda.CUDAGraph()
+name = None
+with torch.cuda.graph(g):
+    try:
+        gx.step_noalloc(du, x, dv, 0, P)
+    except gx.GxGemmError as e:
+        name = e.name
+ref = du.clone()
+gx.step(ref, x, dv, 0, P)
+gx.step_noalloc(du, x, dv, 0, P)   # outside the capture the first call sets the array up and runs
+torch.cuda.synchronize()
+print(json.dumps({"in_capture": name, "same": bool(torch.equal(du, ref)), "err": gx.device_error(clear=True)}))
+"""
+
+
+def test_noalloc_first_call_in_capture_is_refused():
+    """A process whose first allocation-free call comes during stream capture gets SDM_GX_E_CAPTURE (the one-time set-up
+    would break the capture) and nothing else happens; the next call outside the capture sets the array up and gives
+    the stateless call's bits. Run in a child process, whose array is not set up yet."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CAPTURE_CHILD], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out == {"in_capture": "SDM_GX_E_CAPTURE", "same": True, "err": 0}, out
