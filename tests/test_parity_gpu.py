@@ -214,6 +214,23 @@ def test_offset_bases_every_offset_config(shape, offs):
     assert e.value.name == "SDM_GX_E_FLAGS"
 
 
+@pytest.mark.parametrize("vset", synth.VALUE_SETS)
+def test_offset_configs_value_sets(vset):
+    """Every offset configuration, forced, on every value set (zeros and signed zeros, 1e30 magnitudes, wide exponents,
+    denormals, +-Inf and NaN sprinkled in): bases 4 bytes past a 16-byte boundary, a shape with several row and column
+    tiles and a ragged last stage, compared with the oracle bit for bit (NaN as a class)."""
+    w = synth.Workload("offset_vsets", 80, T=2, P=2, C=100, hd=136, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w, value_set=vset)
+    want, _ = _oracle_steps(inp, w.P, [1, 0])
+    for k in _offset_configs():
+        du, dx, dv = _dev(inp, offset=1)
+        pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(k))
+        pl.run(1, -1, pdl=True)
+        torch.cuda.synchronize()
+        assert_bitwise(du.host(), want, f"offset config {k} on {vset}")
+        assert du.guards_intact()
+
+
 def test_offset_bases_large_shape():
     """The large shape (P = 256, C = hd = 128) with every base 4 bytes past a 16-byte boundary: two full steps through
     the plan's offset configuration, compared everywhere."""
