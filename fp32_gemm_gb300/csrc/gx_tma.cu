@@ -1,6 +1,7 @@
-// The TMA-fed, warp-specialised FP32 kernels of the gx_gemm step update (sm_103a): the tile kernel (gx_tma_kernel),
-// the balanced slab kernel (gx_slab_kernel) and the stream kernel (gx_stream_kernel), which share the pipeline, the
-// chain and the epilogue described here and differ in how a step's work is cut over the CTAs.
+// The TMA-fed, warp-specialised FP32 kernels of the gx_gemm step update (sm_103a): the tile kernel (gx_tma_kernel, with
+// offset variants for operand bases off a 16-byte boundary, OCfg), the balanced slab kernel (gx_slab_kernel) and the
+// stream kernel (gx_stream_kernel), which share the pipeline, the chain and the epilogue described here and differ in
+// how a step's work is cut over the CTAs.
 //
 // What it computes (sparse_delta_memory/cuda/gx_gemm_cuda.py, module docstring formula and gx_gemm_kernel): for every
 // chunk n of the step, row i < C and column c < hd, one thread runs acc = +0; acc = fmaf(x[n,j,i], d_dv[n,j,c], acc)
