@@ -363,7 +363,9 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
             if (!usable(k) || tma_config(k).kind == 1 || tma_config(k).kind == 2) continue;
             const ConfigInfo &ci = tma_config(k);
             const int64_t t = tiles_of(ci);
-            if (t > d.sms) continue;
+            // one wave: a tile per SM, or two one-warp CTAs (64 threads; two share an SM at no cost: 64 x 32 x 16
+            // on 256 tiles of 8 x 32 took 1.83 us a step, on 128 tiles of 16 x 32 2.07)
+            if (t > (ci.consumer_warps == 1 ? 2 * static_cast<int64_t>(d.sms) : d.sms)) continue;
             const ConfigInfo &cb = tma_config(bk < 0 ? k : bk);
             const int area = ci.TI * ci.TC, barea = cb.TI * cb.TC;
             if (bk < 0 || t > bt || (t == bt && (area < barea || (area == barea && ci.eff > cb.eff)))) {

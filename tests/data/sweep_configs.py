@@ -3,12 +3,13 @@ not a test): each plan runs a CUDA graph of 8 PDL-chained steps of P chunks, 3 w
 bracketed by CUDA events. One JSON line per shape: P, C, hd, the pick and its time, and the time of every configuration
 the shape admits (microseconds per step). The inputs are N(0, 0.1) x, N(0, 1) d_dv and d_u, contiguous.
 
-    python tests/data/sweep_configs.py [small_c|wide|large_c] > out.jsonl
+    python tests/data/sweep_configs.py [small_c|wide|large_c|narrow] > out.jsonl
 
 small_c: C in {64, 96} x hd in {64, 96, 128} x P in {48 .. 600}; wide: C in {32, 48, 128} x hd in {64, 128} x
-P in {100 .. 800}; large_c: C in {192, 256} x hd in {64, 128, 256} x P in {16, 64, 200}. config_sweep_gb300.jsonl holds
-the first two sets and config_sweep_gb300_large_c.jsonl the third (the tile, slab and stream configurations), as
-measured on one GB300."""
+P in {100 .. 800}; large_c: C in {192, 256} x hd in {64, 128, 256} x P in {16, 64, 200}; narrow: C in {16, 32, 64} x
+hd in {16, 32} x P in {64, 256, 1024}. config_sweep_gb300.jsonl holds
+the first two sets, config_sweep_gb300_large_c.jsonl and config_sweep_gb300_narrow.jsonl the others (the tile, slab
+and stream configurations), as measured on one GB300."""
 import json
 import os
 import sys
@@ -42,6 +43,8 @@ def shapes(which):
         return [(P, C, hd) for C in (32, 48, 128) for hd in (64, 128) for P in (100, 200, 400, 800)]
     if which == "large_c":
         return [(P, C, hd) for C in (192, 256) for hd in (64, 128, 256) for P in (16, 64, 200)]
+    if which == "narrow":
+        return [(P, C, hd) for C in (16, 32, 64) for hd in (16, 32) for P in (64, 256, 1024)]
     return [(P, C, hd) for C in (64, 96) for hd in (64, 96, 128) for P in (48, 100, 160, 220, 300, 400, 600)]
 
 
