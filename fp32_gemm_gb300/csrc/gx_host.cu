@@ -343,8 +343,8 @@ int choose_tma_config(const DevState &d, int64_t P, int64_t C, int64_t hd, int f
                !(ci.kind == 1 && !d.slab_ok) && tiles_of(ci) < kTwo31;
     };
     // Small steps (no tile of 32+ outputs per thread fills the SMs): the step is bound by latency, and the measured
-    // best is the configuration with the most tiles that still fit one wave (one tile per SM), i.e. the most
-    // parallel chains of the least work each. Among equally many tiles the smaller tile wins (a CTA's time follows
+    // best is the tile configuration with the most tiles that still fit one wave (a tile per SM, or two one-warp
+    // CTAs), i.e. the most parallel chains of the least work each. Among equally many tiles the smaller tile wins (a CTA's time follows
     // its tile's area, rows and columns past C and hd included: 128 x 64 tiles on C = 64 took 5.8 us a step where
     // 64 x 64 tiles took 4.2), then the more efficient configuration.
     // (A property of the step's shape, decided on the aligned tile kernels whatever the layout: the offset menu has no
