@@ -22,8 +22,6 @@
 //     point of coherence). d_dv is loaded into shared memory only after the wait; d_u is written only after it.
 //   * Every mbarrier wait is bounded (globaltimer); on expiry the thread sets a bit in the device error word and the
 //     CTA unwinds; the producer first waits (bounded) for the copies it issued.
-#include <utility>
-
 #include "gx_device.cuh"
 #include "gx_internal.h"
 
@@ -37,7 +35,6 @@ struct TCfg {
     static constexpr int EFF = EFF_;               // measured FMA-pipe efficiency at full occupancy, percent
     static constexpr int SLAB = 0;
     static constexpr bool ROWS_OUTER = false;      // FMA order within one j: column-outer (see chain_j)
-    static constexpr bool DUPRE = false;           // stream kernel only: d_u read into registers in the last stage
     static constexpr bool ELEM = false;            // offset configurations (OCfg): element loads of wide boxes
     static constexpr bool SHIFT = false;           // offset configurations (OCfg): tiles on the shifted grid
     static constexpr bool REALIGN = false;         // offset configurations (OCfg): wide boxes realigned per stage
@@ -245,79 +242,6 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
 #pragma unroll
                     for (int e = 0; e < Cfg::VN; ++e)
                         if (c + e >= 0 && c + e < p.hd) grow[c + e] = o[e];
-                }
-            }
-        }
-    }
-}
-
-// The staged d_u vector v (of the thread's SR * VR * SN) into registers: rows ro[sr] + er, columns co[sc] .. + VN - 1.
-template <class Cfg, int V>
-__device__ __forceinline__ void load_du_vec(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                            float (&u)[Cfg::RM][Cfg::RN]) {
-    constexpr int sr = V / (Cfg::VR * Cfg::SN), er = (V / Cfg::SN) % Cfg::VR, sc = V % Cfg::SN;
-    lds<Cfg, Cfg::VN>(us + (ro[sr] + er) * Cfg::UP + co[sc], &u[sr * Cfg::VR + er][sc * Cfg::VN]);
-}
-
-template <class Cfg, int... V>
-__device__ __forceinline__ void load_du_rest(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                             float (&u)[Cfg::RM][Cfg::RN], std::integer_sequence<int, V...>) {
-    (load_du_vec<Cfg, Cfg::DU_PREFETCH_VECS + V>(us, ro, co, u), ...);
-}
-
-template <class Cfg, int... V>
-__device__ __forceinline__ void load_du_all(const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                            float (&u)[Cfg::RM][Cfg::RN], std::integer_sequence<int, V...>) {
-    (load_du_vec<Cfg, V>(us, ro, co, u), ...);
-}
-
-// A full stage whose last NV j each also read one vector of the staged d_u tile into registers (NV = the thread's
-// d_u vectors): the epilogue that follows then needs no shared-memory reads, and the reads overlap the chain.
-template <class Cfg, int U0, int... U>
-__device__ __forceinline__ void chain_tail_du(const float *__restrict__ xs, const float *__restrict__ ds,
-                                              const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                              float (&acc)[Cfg::RM][Cfg::RN], float (&u)[Cfg::RM][Cfg::RN],
-                                              std::integer_sequence<int, U...>) {
-    ((chain_j<Cfg>(xs, ds, U0 + U, ro, co, acc), load_du_vec<Cfg, U>(us, ro, co, u)), ...);
-}
-
-template <class Cfg>
-__device__ __forceinline__ void chain_block_du(const float *__restrict__ xs, const float *__restrict__ ds,
-                                               const float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                               float (&acc)[Cfg::RM][Cfg::RN], float (&u)[Cfg::RM][Cfg::RN]) {
-    constexpr int NV = Cfg::DU_PREFETCH_VECS;
-    static_assert(Cfg::KB >= NV, "a stage holds at least one j per d_u vector");
-#pragma unroll(Cfg::UNROLL)
-    for (int jj = 0; jj < Cfg::KB - NV; ++jj) chain_j<Cfg>(xs, ds, jj, ro, co, acc);
-    chain_tail_du<Cfg, Cfg::KB - NV>(xs, ds, us, ro, co, acc, u, std::make_integer_sequence<int, NV>{});
-}
-
-// The epilogue with d_u already in registers (u): d_u + acc, one rounding each, stored as in epilogue().
-template <class Cfg>
-__device__ __forceinline__ void epilogue_regs(const TmaParams &p, const Tile &tl, const float (&u)[Cfg::RM][Cfg::RN],
-                                              const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
-                                              const float (&acc)[Cfg::RM][Cfg::RN]) {
-#pragma unroll
-    for (int sr = 0; sr < Cfg::SR; ++sr) {
-#pragma unroll
-        for (int er = 0; er < Cfg::VR; ++er) {
-            const int i = tl.i0 + ro[sr] + er;
-            if (i >= p.C) continue;
-            float *grow = p.du + static_cast<int64_t>(tl.n) * p.du_sn + static_cast<int64_t>(i) * p.du_si;
-#pragma unroll
-            for (int sc = 0; sc < Cfg::SN; ++sc) {
-                const int c = tl.c0 + co[sc];
-                if (c >= p.hd) continue;
-                float o[Cfg::VN];
-#pragma unroll
-                for (int e = 0; e < Cfg::VN; ++e)
-                    o[e] = __fadd_rn(u[sr * Cfg::VR + er][sc * Cfg::VN + e], acc[sr * Cfg::VR + er][sc * Cfg::VN + e]);
-                if (c + Cfg::VN <= p.hd) {
-                    dev::Vec<Cfg::VN>::store(grow + c, o);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < Cfg::VN; ++e)
-                        if (c + e < p.hd) grow[c + e] = o[e];
                 }
             }
         }
@@ -608,7 +532,6 @@ struct SCfg {
     static constexpr int SLAB = 1;
     static constexpr int EFF = EFF_;
     static constexpr bool ROWS_OUTER = false;
-    static constexpr bool DUPRE = false;
     static constexpr int RM = 8, RN = 4, KB = KB_, ST = ST_;
     static constexpr int WS = 4, WN = 4;           // slabs per round, warps per slab
     static constexpr int LM = 4, LN = 8;
@@ -892,13 +815,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
 // used the workspace in its own control word, which its publisher warp reads and advances right after the
 // grid-dependency wait (the next launch reads it only after this one has completed; every CTA of every launch counts,
 // so all CTAs agree on the epoch). A flag left by an earlier launch, or by an aborted one, therefore never matches.
-template <class T, int EFF_, bool RO_ = false, bool DUPRE_ = false, int UNROLL_ = T::UNROLL>
+template <class T, int EFF_, bool RO_ = false, int UNROLL_ = T::UNROLL>
 struct KCfg : T {
     static constexpr int SLAB = 2;
     static constexpr int EFF = EFF_;
     static constexpr bool ROWS_OUTER = RO_;
-    static constexpr bool DUPRE = DUPRE_;   // d_u read into registers during a tile's last stage (spare registers)
-    static constexpr int DU_PREFETCH_VECS = (T::SR * T::VR * T::SN) / 2;   // of them, during the stage (register cap)
     static constexpr int UNROLL = UNROLL_;
     static constexpr int THREADS = (T::NCW + 2) * 32;         // consumers, producer, publisher
     static constexpr int OFF_P = T::OFF_BAR;                  // the incoming partial sums [TI][TC]
@@ -1152,7 +1073,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     int it = 0;
     int du_used = 0;
     bool failed = false;
-    float upre[Cfg::DUPRE ? Cfg::RM : 1][Cfg::DUPRE ? Cfg::RN : 1];   // d_u of the tile being finished (DUPRE)
     for (int q = 0; q < R.count && !failed; ++q) {
         const Piece P = piece_at(R, p.C, q);
         const Tile tl = decode_tile<Cfg>(p, P.t);
@@ -1191,32 +1111,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             const float *xs = reinterpret_cast<const float *>(base_g + s * Cfg::XS_BYTES);
             const float *ds = reinterpret_cast<const float *>(base_g + Cfg::OFF_D + s * Cfg::DS_BYTES);
             const int nj = P.j1 - (j0 + kb * Cfg::KB);
-            if constexpr (Cfg::DUPRE) {
-                if (kb == nkb - 1 && P.kind != 1) {
-                    // the tile's last stage: its d_u (staged by then, normally long before) is read into registers
-                    // while the chain runs
-                    if (!__all_sync(0xffffffffu,
-                                    dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
-                        failed = true;
-                        break;
-                    }
-                    if (nj >= Cfg::KB) {
-                        chain_block_du<Cfg>(xs, ds, us, ro, co, acc, upre);
-                    } else {
-                        load_du_all<Cfg>(us, ro, co, upre, std::make_integer_sequence<int, Cfg::DU_PREFETCH_VECS>{});
-                        chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
-                    }
-                } else if (nj >= Cfg::KB) {
-                    chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
-                } else {
-                    chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
-                }
+            if (nj >= Cfg::KB) {
+                chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
             } else {
-                if (nj >= Cfg::KB) {
-                    chain_block<Cfg, true>(xs, ds, ro, co, acc, Cfg::KB);
-                } else {
-                    chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
-                }
+                chain_block<Cfg, false>(xs, ds, ro, co, acc, nj);
             }
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(bar0 + 8u * (Cfg::ST + s));
@@ -1230,19 +1128,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             if (lane == 0) dev::mbar_arrive(head_staged);
             continue;
         }
-        if constexpr (Cfg::DUPRE) {
-            // the vectors not read during the last stage come from shared memory now
-            load_du_rest<Cfg>(us, ro, co, upre,
-                              std::make_integer_sequence<int, Cfg::SR * Cfg::VR * Cfg::SN - Cfg::DU_PREFETCH_VECS>{});
-            epilogue_regs<Cfg>(p, tl, upre, ro, co, acc);
-        } else {
-            if (!__all_sync(0xffffffffu,
-                            dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
-                failed = true;
-                break;
-            }
-            epilogue<Cfg>(p, tl, us, ro, co, acc);
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(du_full, static_cast<uint32_t>(du_used) & 1u, p.timeout_ns))) {
+            failed = true;
+            break;
         }
+        epilogue<Cfg>(p, tl, us, ro, co, acc);
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(du_empty);
         ++du_used;
@@ -1308,10 +1198,10 @@ using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 war
 using C12 = KCfg<C0, 72>;                     // C0's tile with the (tile, j) work split evenly over the CTAs
 using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128 x 64 tiles, 8 warps, 2 CTAs per SM
 // The split on 128 x 128 tiles with 8 consumer warps of 8 x 8 (rows-outer FMA order, KB = 32, 3 stages, 224 KB of
-// shared memory): a third fewer shared loads per FMA (its chains run ~6% faster than C12's on the large step), half
-// of the tile's d_u read into spare registers during the tile's last stage; its epilogues cost more with 8 warps, so
-// the large step comes out even (22.3 us per step either way). The rule prefers C12; autotune measures both.
-using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, true, 16>;
+// shared memory, 127 registers): a third fewer shared loads per FMA than C12. Measured on the large step (256 tiles
+// on 152 SMs) at 21.8-21.9 us against C12's 22.3; reading half of each tile's d_u into registers during its last
+// stage (161 registers) made it 22.1 us.
+using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, 16>;
 
 // The tile kernel for operands whose rows start 4, 8 or 12 bytes past a 16-byte boundary (a 4-byte-aligned base with
 // strides that are multiples of 16 bytes: a slice at an odd offset, say). TMA needs 16-byte-aligned bases and innermost

@@ -31,6 +31,7 @@ def test_description_matches_the_menu():
 def test_large_step_takes_the_stream_kernel_with_a_workspace():
     k = pick(256, 128, 128)
     assert info(k)["kind"] == "stream" and (info(k)["TI"], info(k)["TC"]) == (128, 128)
+    assert info(k)["consumer_warps"] == 8   # 8 x 8 outputs a thread: measured 21.8-21.9 us against 22.3 for 8 x 4
     k0 = pick(256, 128, 128, ws=0)   # without a workspace: the 128 x 128 tile kernel
     assert info(k0)["kind"] == "tile" and (info(k0)["TI"], info(k0)["TC"], info(k0)["consumer_warps"]) == (128, 128, 16)
 
@@ -100,31 +101,38 @@ def _sweep(name="config_sweep_gb300.jsonl"):
         return [json.loads(line) for line in f if line.strip()]
 
 
+def _excess(r, k):
+    """The measured step time of pick k over the fastest configuration the rule may take for these contiguous operands
+    (the sweep also times the offset configurations, forced, which serve only operand bases off a 16-byte boundary)."""
+    aligned = [v for kk, v in r["us"].items() if info(int(kk))["kind"] in ("tile", "slab", "stream")]
+    return r["us"][str(k)] / min(aligned) - 1.0
+
+
 def test_rule_against_the_measured_sweep():
     """The rule's pick on each of 66 shapes (C 32 .. 128, hd 64 .. 128, P 48 .. 800), against every configuration
     timed on one GB300 (tests/data/config_sweep_gb300.jsonl, written by tests/data/sweep_configs.py): the pick is one
-    the shape admits, and its measured step time is close to the fastest. The bounds hold the fitted model's result
-    (mean 1.0 % and worst 7.8 % over the fastest at C = 64 and 96; 2.0 % and 11.9 % at C = 32, 48 and 128, where the
-    close calls sit between configurations within a few tenths of a microsecond); the earlier whole-round estimate
-    scored 7.1 % / 41.9 % on the first set."""
+    the shape admits, and its measured step time is close to the fastest. The bounds hold the fitted model's result on
+    this recording (mean 1.1 % and worst 7.7 % over the fastest at C = 64 and 96, 38 of 42 within 5 %; 2.0 % and
+    12.3 % at C = 32, 48 and 128, where the close calls sit between configurations within a few tenths of a
+    microsecond); the earlier whole-round estimate scored 7.1 % / 41.9 % on the first set."""
     rows = _sweep()
     assert len(rows) == 66
     excess = {True: [], False: []}
     for r in rows:
         k = pick(r["P"], r["C"], r["hd"])
         assert str(k) in r["us"], (r["P"], r["C"], r["hd"], k)
-        excess[r["C"] in (64, 96)].append(r["us"][str(k)] / min(r["us"].values()) - 1.0)
+        excess[r["C"] in (64, 96)].append(_excess(r, k))
     small, wide = excess[True], excess[False]
     assert len(small) == 42 and len(wide) == 24
     assert sum(small) / len(small) <= 0.015 and max(small) <= 0.08
-    assert sum(1 for e in small if e <= 0.05) >= 39
+    assert sum(1 for e in small if e <= 0.05) >= 38
     assert sum(wide) / len(wide) <= 0.025 and max(wide) <= 0.125
 
 
 def test_rule_against_the_large_c_sweep():
     """The same against 18 shapes with C = 192 and 256 (hd 64 .. 256, P 16 .. 200; the tile, slab and stream
     configurations timed on one GB300, tests/data/config_sweep_gb300_large_c.jsonl, the large_c set of
-    tests/data/sweep_configs.py): mean 1.9% and worst 9.5% over the fastest (before the slab kernel was kept out of the
+    tests/data/sweep_configs.py): mean 1.7% and worst 9.3% over the fastest (before the slab kernel was kept out of the
     latency-bound branch: 4.8% and 28%)."""
     rows = _sweep("config_sweep_gb300_large_c.jsonl")
     assert len(rows) == 18
@@ -132,19 +140,19 @@ def test_rule_against_the_large_c_sweep():
     for r in rows:
         k = pick(r["P"], r["C"], r["hd"])
         assert str(k) in r["us"], (r["P"], r["C"], r["hd"], k)
-        excess.append(r["us"][str(k)] / min(r["us"].values()) - 1.0)
+        excess.append(_excess(r, k))
     assert sum(excess) / len(excess) <= 0.025 and max(excess) <= 0.10
 
 
 def test_rule_against_the_narrow_sweep():
     """The same against 18 narrow shapes (C 16 .. 64, hd 16 and 32, P 64 .. 1024;
-    tests/data/config_sweep_gb300_narrow.jsonl, the narrow set of tests/data/sweep_configs.py): mean 0.9% and worst
-    10.3% over the fastest (one wave of one-warp CTAs counts two an SM: 3.5% and 14% before)."""
+    tests/data/config_sweep_gb300_narrow.jsonl, the narrow set of tests/data/sweep_configs.py): mean 0.6% and worst
+    5.6% over the fastest (one wave of one-warp CTAs counts two an SM: 3.5% and 14% on an earlier recording)."""
     rows = _sweep("config_sweep_gb300_narrow.jsonl")
     assert len(rows) == 18
     excess = []
     for r in rows:
         k = pick(r["P"], r["C"], r["hd"])
         assert str(k) in r["us"], (r["P"], r["C"], r["hd"], k)
-        excess.append(r["us"][str(k)] / min(r["us"].values()) - 1.0)
-    assert sum(excess) / len(excess) <= 0.015 and max(excess) <= 0.11
+        excess.append(_excess(r, k))
+    assert sum(excess) / len(excess) <= 0.015 and max(excess) <= 0.08
