@@ -39,11 +39,22 @@ def test_expired_waits_are_reported_and_the_context_survives():
     assert np.isfinite(du2.host()).all()
 
 
-def test_stream_kernel_expired_waits_are_reported():
+def _stream_config(thread_tile):
+    """The stream configuration with 128 x 128 tiles and one CTA per SM whose threads hold thread_tile outputs (8 x 4:
+    16 consumer warps; 8 x 8: 8, the large step's)."""
+    warps = {"8x4": 16, "8x8": 8}[thread_tile]
+    ks = [c for c in range(gx.num_configs(1)) if gx.config_info(1, c)["kind"] == "stream"
+          and gx.config_info(1, c)["TC"] == 128 and gx.config_info(1, c)["consumer_warps"] == warps]
+    assert len(ks) == 1, ks
+    return ks[0]
+
+
+@pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
+def test_stream_kernel_expired_waits_are_reported(thread_tile):
     """The same hook on the stream kernel (one CTA per SM, chains handed between CTAs through the plan's workspace):
     both stalled launches complete with the error word set, the context stays usable, and a stream-kernel plan on
     fresh buffers then matches the oracle over two passes of its steps."""
-    k = [c for c in range(gx.num_configs(1)) if gx.config_info(1, c)["kind"] == "stream"][0]
+    k = _stream_config(thread_tile)
     w = synth.Workload("stall_stream", 71, T=2, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     du, dx, dv = (DevArray(inp[k_]) for k_ in ("d_u", "x", "d_dv"))
@@ -67,13 +78,14 @@ def test_stream_kernel_expired_waits_are_reported():
     assert gx.device_error(clear=True) == 0
 
 
-def test_stream_kernel_late_handoff_recomputes_exactly():
+@pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
+def test_stream_kernel_late_handoff_recomputes_exactly(thread_tile):
     """A hand-off that never comes (the test hook makes every CTA store but never flag its head's partial sums): each
     tail's wait runs out after its 1 ms bound and the CTA computes that tile's whole chain itself. The steps' results
     are still oracle-exact, the device error word carries only the informational bit 3 (device_error returns it without
     a fault status), and a normal launch on the same workspace afterwards is exact too (the flags it finds are stale,
     and the launch epochs tell)."""
-    k = [c for c in range(gx.num_configs(1)) if gx.config_info(1, c)["kind"] == "stream"][0]
+    k = _stream_config(thread_tile)
     w = synth.Workload("late_handoff", 78, T=2, P=160, C=64, hd=64, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     du, dx, dv = (DevArray(inp[k_]) for k_ in ("d_u", "x", "d_dv"))

@@ -592,19 +592,26 @@ def test_run_host_overlapped_copies():
     assert_bitwise(host["x"].numpy(), inp["x"], "x host unchanged")
 
 
-def _stream_config():
-    return [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "stream"][0]
+def _stream_config(thread_tile="8x8"):
+    """The stream configuration with 128 x 128 tiles and one CTA per SM whose threads hold thread_tile outputs: 8 x 8
+    (8 consumer warps, the large step's) or 8 x 4 (16 consumer warps)."""
+    warps = {"8x4": 16, "8x8": 8}[thread_tile]
+    ks = [k for k in range(gx.num_configs(1)) if gx.config_info(1, k)["kind"] == "stream"
+          and gx.config_info(1, k)["TC"] == 128 and gx.config_info(1, k)["consumer_warps"] == warps]
+    assert len(ks) == 1, ks
+    return ks[0]
 
 
+@pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
 @pytest.mark.parametrize("P,C,hd,T", [(160, 100, 76, 2), (153, 64, 64, 2), (100, 128, 200, 2), (304, 128, 128, 2),
                                       (200, 32, 500, 2), (256, 128, 128, 2), (1000, 32, 64, 2), (160, 256, 128, 2)])
-def test_stream_kernel_shapes(P, C, hd, T):
+def test_stream_kernel_shapes(P, C, hd, T, thread_tile):
     """The stream kernel (a step's (tile, j) work split evenly over one CTA per SM; chains continued across CTAs from
     the accumulators left in the plan's workspace): ragged rows and columns, one tile more than SMs (hand-offs with
     almost no slack), several column blocks, exactly two tiles per CTA (no split), the large step, many whole tiles
     per CTA (1000 tiles), and C = 256 (two row blocks per chunk). The chain is captured into a graph and replayed
-    twice, so the workspace's launch epoch advances over 2T launches."""
-    k = _stream_config()
+    twice, so the workspace's launch epoch advances over 2T launches. Both 128 x 128 thread tilings."""
+    k = _stream_config(thread_tile)
     w = synth.Workload("stream", 68, T=T, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
     inp = synth.make_inputs(w)
     want, _ = _oracle_steps(inp, P, list(range(T - 1, -1, -1)) * 2)
@@ -710,12 +717,13 @@ def test_run_host_stream_kernel():
     assert_bitwise(host["d_u"].numpy(), want, "run_host stream kernel x2")
 
 
+@pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
 @pytest.mark.parametrize("vset", synth.VALUE_SETS)
-def test_stream_kernel_value_sets(vset):
+def test_stream_kernel_value_sets(vset, thread_tile):
     """The stream kernel on every value set (zeros and signed zeros, 1e30-scale overflow, the wide range, subnormals,
     +-Inf, NaN): the FP32 accumulators handed between CTAs through shared memory, bulk copies and the workspace keep
     their bits (NaN as a class), and no output is -0. 160 chunks of 48 x 100: every hand-off is tight."""
-    k = _stream_config()
+    k = _stream_config(thread_tile)
     w = synth.Workload("stream_vs", 75, T=2, P=160, C=48, hd=100, x_scale="unit")
     inp = synth.make_inputs(w, value_set=vset)
     want, _ = _oracle_steps(inp, w.P, [0, 1])
