@@ -717,6 +717,44 @@ def test_run_host_stream_kernel():
     assert_bitwise(host["d_u"].numpy(), want, "run_host stream kernel x2")
 
 
+def _random_stream_shapes(n, seed, sms=152):
+    """n step shapes (P, C, hd) on which a 128 x 128 stream configuration with one CTA per SM is admitted: C and hd
+    multiples of 4 (TMA rows), 1 or 2 row blocks and 1 to 3 column blocks per chunk, between one and four tiles a CTA."""
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        C = 4 * rng.randint(1, 64)
+        hd = 4 * rng.randint(1, 96)
+        per_chunk = -(-C // 128) * -(-hd // 128)
+        P = -(-rng.randint(sms, 4 * sms) // per_chunk)
+        if sms <= P * per_chunk <= 16 * sms:
+            out.append((P, C, hd))
+    return out
+
+
+@pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
+@pytest.mark.parametrize("shape", _random_stream_shapes(6, 2026))
+def test_stream_kernel_random_shapes(shape, thread_tile):
+    """Seeded random shapes through the stream kernel (any split point, ragged rows and columns in any tile, one to
+    three column blocks, tight and loose hand-offs), two chained steps forward then back, bit-exact against the
+    oracle; the guard bands around d_u stay intact and x and d_dv are not written."""
+    P, C, hd = shape
+    k = _stream_config(thread_tile)
+    w = synth.Workload("stream_rand", 80 + P % 7, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, [0, 1, 1, 0])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(k))
+    assert pl.geometry()["config"] == k
+    pl.run(0, 2, pdl=True)
+    pl.run(1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"stream {thread_tile} P={P} C={C} hd={hd}")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, "stream random")
+
+
 @pytest.mark.parametrize("thread_tile", ["8x4", "8x8"])
 @pytest.mark.parametrize("vset", synth.VALUE_SETS)
 def test_stream_kernel_value_sets(vset, thread_tile):
