@@ -798,8 +798,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
 // ---- the stream kernel: the tile kernel with the step's (tile, j) work split evenly over the CTAs ----------------------
 // Every output's chain runs over j = 0..C-1 in order, but nothing requires one CTA to run all of it: a chain stopped
 // after some j and continued later from the same FP32 accumulator value gives the same bits. So the step's work is laid
-// out as W = tiles x C units (tile t, j) in the order (t, j), and CTA b takes units [b W / G, (b + 1) W / G): the SMs
-// get the same work to within one j, where whole tiles leave 104 of 152 SMs with a second tile on the large shape.
+// out as W = tiles x C units (tile t, j) in the order (t, j), and CTA b takes a contiguous range of them, an equal
+// share of the step's cost (the units plus a charge for each tile boundary inside a range, cta_pieces): the SMs get
+// the same work to within that charge, where whole tiles leave 104 of 152 SMs with a second tile on the large shape.
 // With W / G >= C (the host's condition) a CTA's range is, in order, the tail of a tile whose leading j belong to CTA
 // b - 1, some whole tiles, and the leading j of a tile whose tail belongs to CTA b + 1 (cta_pieces). It runs them as
 //   1. the head piece first: the first je values of j of its last tile, from +0. The consumer warps leave their
