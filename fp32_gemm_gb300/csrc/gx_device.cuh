@@ -107,8 +107,19 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
                  "r"(src), "r"(bytes)
                  : "memory");
 }
+// 3-D tiled store of one box from this CTA's shared memory to global memory, committed as its own bulk group.
+// Elements of the box outside the tensor's extents are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(src)
+        : "memory");
+}
 // waits until every bulk group this thread committed has completed (its writes performed)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// waits until every bulk group this thread committed has read its shared-memory source (which may then be reused)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // ---- flags between CTAs (global memory, GPU scope) ---------------------------------------------------------------------
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {

@@ -248,6 +248,29 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
     }
 }
 
+// The epilogue of a tile stored by TMA (stream kernel, TMID): d_u + acc, one rounding each, written back over the
+// staged d_u tile us[TI][TC] at the thread's own positions. Rows and columns outside the operands are written too (on
+// zero-filled d_u); the TMA store leaves them out.
+template <class Cfg>
+__device__ __forceinline__ void epilogue_to_smem(float *us, const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
+                                                 const float (&acc)[Cfg::RM][Cfg::RN]) {
+#pragma unroll
+    for (int sr = 0; sr < Cfg::SR; ++sr) {
+#pragma unroll
+        for (int er = 0; er < Cfg::VR; ++er) {
+#pragma unroll
+            for (int sc = 0; sc < Cfg::SN; ++sc) {
+                float *q = us + (ro[sr] + er) * Cfg::UP + co[sc];
+                float u[Cfg::VN], o[Cfg::VN];
+                dev::Vec<Cfg::VN>::load(q, u);
+#pragma unroll
+                for (int e = 0; e < Cfg::VN; ++e) o[e] = __fadd_rn(u[e], acc[sr * Cfg::VR + er][sc * Cfg::VN + e]);
+                dev::Vec<Cfg::VN>::store(q, o);
+            }
+        }
+    }
+}
+
 // Realigning offset configurations: warp w shifts rows w, w + NCW, .. of the stage's x box [KB][TI + 4] (then of its
 // d_dv box [KB][TC + 4]) left by the operand's offset (0..3 floats) into the aligned buffers xa [KB][TI], da [KB][TC].
 // A row is one warp-wide pass: lane l reads the box row's 16-byte vector l, takes the next one from lane l + 1 (lane
@@ -811,22 +834,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) gx_slab_kernel(const __grid_c
 //   3. the tail piece last: the producer waits (bounded) for CTA b - 1's flag, copies that CTA's partial sums into a
 //      shared buffer of their own with one bulk copy, and the consumers continue the chain from them at j = ja, then
 //      add d_u.
+// TMID: a tile the CTA finishes before its last piece is not stored by the consumers: they write d_u + acc back over
+// the staged d_u tile and go on at once, and the publisher warp stores it with one TMA store, handing the d_u buffer
+// back to the producer once the store has read it. The CTA's last tile keeps the consumers' own stores, so that no
+// store's completion lies between the CTA's last FMA and its end.
 // CTA b - 1 finishes its head piece after ja units of work; CTA b starts its tail after (W / G) - (C - ja) >= ja units,
 // so the hand-off is normally ready long before it is needed. Flags carry an epoch: each CTA counts the launches that
 // used the workspace in its own control word, which its publisher warp reads and advances right after the
 // grid-dependency wait (the next launch reads it only after this one has completed; every CTA of every launch counts,
 // so all CTAs agree on the epoch). A flag left by an earlier launch, or by an aborted one, therefore never matches.
-template <class T, int EFF_, bool RO_ = false, int UNROLL_ = T::UNROLL>
+template <class T, int EFF_, bool RO_ = false, int UNROLL_ = T::UNROLL, bool TMID_ = false>
 struct KCfg : T {
     static constexpr int SLAB = 2;
     static constexpr int EFF = EFF_;
     static constexpr bool ROWS_OUTER = RO_;
     static constexpr int UNROLL = UNROLL_;
+    static constexpr bool TMID = TMID_;   // tiles finished before the CTA's last piece: stored by TMA (see above)
     static constexpr int THREADS = (T::NCW + 2) * 32;         // consumers, producer, publisher
     static constexpr int OFF_P = T::OFF_BAR;                  // the incoming partial sums [TI][TC]
     static constexpr int OFF_BAR = OFF_P + T::DU_BYTES;
-    // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known
-    static constexpr int NBAR = 2 * T::ST + 6;
+    // stages full / empty, d_u full / empty, partial full, head staged, head stored, epoch known, tile staged
+    static constexpr int NBAR = 2 * T::ST + 7;
     static constexpr int OFF_EPOCH = OFF_BAR + NBAR * 8;      // this launch's epoch, from the publisher to the producer
     static constexpr int OFF_RECOMP = OFF_EPOCH + 4;          // 1: the tail piece recomputes its tile (late hand-off)
     static constexpr int OFF_PIECES = align_up(OFF_RECOMP + 4, 16);   // the CTA's Pieces (computed once)
@@ -882,6 +910,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
     const uint32_t head_staged = part_full + 8u;   // NCW arrivals: the head's accumulators are in the d_u buffer
     const uint32_t head_stored = head_staged + 8u; // 1 arrival: the publisher's bulk store has read them
     const uint32_t epoch_known = head_stored + 8u; // 1 arrival: the publisher has put the epoch in shared memory
+    const uint32_t tile_staged = epoch_known + 8u; // NCW arrivals: a tile for the publisher's TMA store (TMID)
     volatile uint32_t *const epoch_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_EPOCH);
     volatile uint32_t *const recomp_s = reinterpret_cast<volatile uint32_t *>(base_g + Cfg::OFF_RECOMP);
     const int warp = vt / 32;
@@ -895,11 +924,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             dev::mbar_init(bar0 + 8u * (Cfg::ST + s), Cfg::NCW);
         }
         dev::mbar_init(du_full, 1);
-        dev::mbar_init(du_empty, Cfg::NCW);
+        // TMID: only the publisher frees the d_u buffer (after each TMA store has read it); the last tile's buffer is
+        // never needed again
+        dev::mbar_init(du_empty, Cfg::TMID ? 1 : Cfg::NCW);
         dev::mbar_init(part_full, 1);
         dev::mbar_init(head_staged, Cfg::NCW);
         dev::mbar_init(head_stored, 1);
         dev::mbar_init(epoch_known, 1);
+        dev::mbar_init(tile_staged, Cfg::NCW);
         dev::fence_mbar_init();
         *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G, p.stream_kappa);
     }
@@ -928,6 +960,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
                 atomicOr(p.err, kErrConsumerWait);
             }
             dev::mbar_arrive(head_stored);   // the d_u buffer is free again (also after a failed wait: no copy ran)
+        }
+        if constexpr (Cfg::TMID) {
+            // the tiles the CTA finishes before its last piece (every piece after the head but the last)
+            int k = 0;
+            for (int q = R.has_head; q < R.count - 1; ++q, ++k) {
+                const Tile tl = decode_tile<Cfg>(p, piece_at(R, p.C, q).t);
+                if (!dev::mbar_wait(tile_staged, static_cast<uint32_t>(k) & 1u, p.timeout_ns)) {
+                    atomicOr(p.err, kErrConsumerWait);
+                    break;
+                }
+                dev::tma_store_3d(&p.tm_du, tl.c0, tl.i0, tl.n, base_s + Cfg::OFF_U);
+                dev::bulk_wait_read_all();
+                dev::mbar_arrive(du_empty);
+            }
+            dev::bulk_wait_all();   // every store performed before the CTA ends
         }
         return;
     }
@@ -1133,9 +1180,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
             failed = true;
             break;
         }
-        epilogue<Cfg>(p, tl, us, ro, co, acc);
-        __syncwarp();
-        if (lane == 0) dev::mbar_arrive(du_empty);
+        if (Cfg::TMID && q < R.count - 1) {
+            epilogue_to_smem<Cfg>(us, ro, co, acc);
+            dev::fence_proxy_async_smem();   // the values are read by the publisher's TMA store
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(tile_staged);
+        } else {
+            epilogue<Cfg>(p, tl, us, ro, co, acc);
+            __syncwarp();
+            if (!Cfg::TMID && lane == 0) dev::mbar_arrive(du_empty);
+        }
         ++du_used;
     }
     if (failed && lane == 0) atomicOr(p.err, kErrConsumerWait);
@@ -1199,10 +1253,12 @@ using C11 = SCfg<32, 3, 72>;                  // balanced 32 x 128 slabs, 16 war
 using C12 = KCfg<C0, 72>;                     // C0's tile with the (tile, j) work split evenly over the CTAs
 using C13 = KCfg<TCfg<8, 4, 4, 2, 16, 4, 2, 70>, 68>;   // the same split on 128 x 64 tiles, 8 warps, 2 CTAs per SM
 // The split on 128 x 128 tiles with 8 consumer warps of 8 x 8 (rows-outer FMA order, KB = 32, 3 stages, 224 KB of
-// shared memory, 127 registers): a third fewer shared loads per FMA than C12. Measured on the large step (256 tiles
-// on 152 SMs) at 21.8-21.9 us against C12's 22.3; reading half of each tile's d_u into registers during its last
-// stage (161 registers) made it 22.1 us.
-using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, 16>;
+// shared memory, 127 registers): a third fewer shared loads per FMA than C12. Its tiles finished before a CTA's last
+// piece go out by TMA store (TMID): with 8 warps the consumers' own stores of a tile took ~1.1 us (too few stores in
+// flight), against ~0.6 us with C12's 16. Measured on the large step (256 tiles on 152 SMs): 21.7 us, against 21.8-21.9
+// without the TMA stores and 22.2-22.3 for C12; reading half of each tile's d_u into registers during its last stage
+// (161 registers) had made it 22.1 us.
+using C14 = KCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 80>, 70, true, 16, true>;
 
 // The tile kernel for operands whose rows start 4, 8 or 12 bytes past a 16-byte boundary (a 4-byte-aligned base with
 // strides that are multiples of 16 bytes: a slice at an odd offset, say). TMA needs 16-byte-aligned bases and innermost
