@@ -309,15 +309,19 @@ double estimate_us(int k, const ConfigInfo &ci, int occ, int sms, int64_t P, int
 // The slab kernel needs whole 32-row slabs (C % 32 == 0) and at most two (chunk, column block) per round of four
 // consecutive slabs (C / 32 >= 3). The stream kernel runs `stream_ctas` CTAs (every resident slot: SMs x CTAs per
 // SM), needs the plan's workspace sized for them (ws_bytes), and at least as many tiles as CTAs, so that every CTA's
-// range of (tile, j) units is at least one tile long. It is offered up to kStreamMaxTilesPerCta tiles a CTA: past
-// that whole tiles leave at most a sixteenth of a round idle, less than the split's own cost per tile (measured: 8192
-// chunks of 128 x 128 x 128, 54 tiles an SM, run 17.9 us a chunk-step on whole tiles, 18.4 split).
+// range of (tile, j) units is at least one tile long. A configuration whose consumers store every tile themselves is
+// offered up to kStreamMaxTilesPerCta tiles a CTA: past that whole tiles leave at most a sixteenth of a round idle,
+// less than the split's own cost per tile (measured with 8 x 4 tiles: 8192 chunks of 128 x 128 x 128, 54 tiles an SM,
+// 584 us a step split against 568 on whole tiles). One that stores the tiles finished before a CTA's last piece by TMA
+// has no such bound: with 8 x 8 tiles it measured 531 us there, and 139 / 200 / 269 us against 152 / 215 / 288 on
+// whole tiles at 2048 / 3000 / 4096 chunks.
 constexpr int64_t kStreamMaxTilesPerCta = 16;
 bool config_eligible(const ConfigInfo &ci, int64_t P, int64_t C, int64_t hd, int stream_ctas, size_t ws_bytes) {
     if (ci.kind == 1) return C % ci.TI == 0 && C / ci.TI >= 3;
     if (ci.kind == 2) {
         const int64_t tiles = P * ((C + ci.TI - 1) / ci.TI) * ((hd + ci.TC - 1) / ci.TC);
-        return stream_ctas >= 1 && tiles >= stream_ctas && tiles <= kStreamMaxTilesPerCta * stream_ctas &&
+        return stream_ctas >= 1 && tiles >= stream_ctas &&
+               (ci.tma_mid || tiles <= kStreamMaxTilesPerCta * stream_ctas) &&
                ws_bytes >= stream_workspace_bytes(stream_ctas, ci.TI, ci.TC);
     }
     return true;

@@ -35,6 +35,7 @@ struct TCfg {
     static constexpr int EFF = EFF_;               // measured FMA-pipe efficiency at full occupancy, percent
     static constexpr int SLAB = 0;
     static constexpr bool ROWS_OUTER = false;      // FMA order within one j: column-outer (see chain_j)
+    static constexpr bool TMID = false;            // stream kernel only (KCfg)
     static constexpr bool ELEM = false;            // offset configurations (OCfg): element loads of wide boxes
     static constexpr bool SHIFT = false;           // offset configurations (OCfg): tiles on the shifted grid
     static constexpr bool REALIGN = false;         // offset configurations (OCfg): wide boxes realigned per stage
@@ -555,6 +556,7 @@ struct SCfg {
     static constexpr int SLAB = 1;
     static constexpr int EFF = EFF_;
     static constexpr bool ROWS_OUTER = false;
+    static constexpr bool TMID = false;
     static constexpr int RM = 8, RN = 4, KB = KB_, ST = ST_;
     static constexpr int WS = 4, WN = 4;           // slabs per round, warps per slab
     static constexpr int LM = 4, LN = 8;
@@ -1232,7 +1234,8 @@ const void *kernel_of() {
 template <class Cfg>
 ConfigInfo info_of() {
     return ConfigInfo{Cfg::TI, Cfg::TC, Cfg::KB, Cfg::ST, Cfg::THREADS, Cfg::SMEM, Cfg::RM, Cfg::RN, Cfg::NCW,
-                      Cfg::EFF, (Cfg::ELEM || Cfg::SHIFT || Cfg::REALIGN) ? 3 : Cfg::SLAB, Cfg::SHIFT ? 1 : 0};
+                      Cfg::EFF, (Cfg::ELEM || Cfg::SHIFT || Cfg::REALIGN) ? 3 : Cfg::SLAB, Cfg::SHIFT ? 1 : 0,
+                      Cfg::TMID ? 1 : 0};
 }
 
 // The tile menu: (RM, RN, WM, WN, KB, ST, MINB, EFF). EFF is a calibrated FMA-pipe efficiency (percent) used by the

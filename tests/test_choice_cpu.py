@@ -36,11 +36,22 @@ def test_large_step_takes_the_stream_kernel_with_a_workspace():
     assert info(k0)["kind"] == "tile" and (info(k0)["TI"], info(k0)["TC"], info(k0)["consumer_warps"]) == (128, 128, 16)
 
 
-def test_many_tiles_per_sm_take_whole_tiles():
-    """Past 16 tiles a CTA the stream kernel is not offered: whole tiles then leave at most a sixteenth of a round idle
-    (8192 chunks of the large shape, 54 tiles an SM: 17.9 us a chunk-step on whole tiles against 18.4 split)."""
-    assert info(pick(8192, 128, 128))["kind"] == "tile"
-    assert info(pick(2048, 128, 128))["kind"] == "stream"   # 13.5 tiles an SM
+def test_many_tiles_per_sm():
+    """The 8 x 8 stream configuration, whose CTAs store the tiles they finish before their last piece by TMA, is offered
+    at any number of tiles a CTA (8192 chunks of the large shape, 54 tiles an SM: 531 us a step against 568 on whole
+    tiles). A stream configuration whose consumers store every tile is offered only up to 16 tiles a CTA (with 8 x 4
+    tiles: 584 us against 568); without the 8 x 8 one (no slot for it on the described device) the rule then takes
+    whole tiles."""
+    for P in (2048, 8192):
+        k = pick(P, 128, 128)
+        assert info(k)["kind"] == "stream" and info(k)["consumer_warps"] == 8, (P, k)
+    k14 = pick(256, 128, 128)
+    occ = list(TMA_OCC)
+    occ[k14] = 0
+    k = gx.choose_config(1, SMS, occ, 8192, 128, 128, ws_bytes=WS)
+    assert info(k)["kind"] == "tile"
+    k = gx.choose_config(1, SMS, occ, 2048, 128, 128, ws_bytes=WS)   # 13.5 tiles an SM
+    assert info(k)["kind"] == "stream" and info(k)["consumer_warps"] == 16
 
 
 @pytest.mark.parametrize("shape,tile", [((32, 64, 128), (32, 64)),    # pdl_chain: 128 tiles of 32 x 64

@@ -717,6 +717,31 @@ def test_run_host_stream_kernel():
     assert_bitwise(host["d_u"].numpy(), want, "run_host stream kernel x2")
 
 
+@pytest.mark.parametrize("P,C,hd", [(2600, 32, 64), (3100, 48, 36)])
+def test_stream_kernel_many_tiles_per_cta(P, C, hd):
+    """The 8 x 8 stream configuration past 16 tiles a CTA (17 and 20 tiles an SM; no bound for the configuration that
+    stores mid-CTA tiles by TMA): two chained steps and the reverse, bit-exact; the 8 x 4 configuration, bounded at 16
+    tiles a CTA, is refused when forced on the same shape."""
+    k = _stream_config("8x8")
+    w = synth.Workload("stream_many", 86, T=2, P=P, C=C, hd=hd, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, P, [0, 1, 1, 0])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(k))
+    g = pl.geometry()
+    assert g["config"] == k and g["tiles"] > 16 * g["ctas"]
+    pl.run(0, 2, pdl=True)
+    pl.step(1, pdl=False)   # not a dependent launch of the step 1 before it (it writes this step's d_u)
+    pl.step(0, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"stream 8x8, {g['tiles']} tiles on {g['ctas']} CTAs")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, "stream many tiles")
+    with pytest.raises(gx.GxGemmError) as e:
+        gx.Plan(du.t, dx.t, dv.t, P, flags=gx.config_flag(_stream_config("8x4")))
+    assert e.value.name == "SDM_GX_E_FLAGS"
+
+
 def _random_stream_shapes(n, seed, sms=152):
     """n step shapes (P, C, hd) on which a 128 x 128 stream configuration with one CTA per SM is admitted: C and hd
     multiples of 4 (TMA rows), 1 or 2 row blocks and 1 to 3 column blocks per chunk, between one and four tiles a CTA."""
