@@ -76,7 +76,7 @@ struct ConfigInfo {
                 // 3: tile kernel for operand bases off a 16-byte boundary (aligned-down tensor maps)
     int shifted;   // kind 3: 0 element loads of boxes 4 floats wider; 1 tiles on the shifted grid
                    // (ceil((C + off_x) / TI) x ceil((hd + off_v) / TC) tiles a chunk; needs off_u == off_v)
-    int tma_mid;   // kind 2: 1 if the tiles a CTA finishes before its last piece are stored by TMA
+    int tma_mid;   // 1 if the tiles a CTA finishes before its last (piece) are stored by TMA (kinds 0 and 2)
 };
 
 // Workspace of the stream kernel for `grid` CTAs of a TI x TC tile: partial sums [grid][TI][TC], one flag per CTA,

@@ -35,7 +35,7 @@ struct TCfg {
     static constexpr int EFF = EFF_;               // measured FMA-pipe efficiency at full occupancy, percent
     static constexpr int SLAB = 0;
     static constexpr bool ROWS_OUTER = false;      // FMA order within one j: column-outer (see chain_j)
-    static constexpr bool TMID = false;            // stream kernel only (KCfg)
+    static constexpr bool TMID = false;            // tiles before a CTA's last stored by TMA (TmCfg, KCfg)
     static constexpr bool ELEM = false;            // offset configurations (OCfg): element loads of wide boxes
     static constexpr bool SHIFT = false;           // offset configurations (OCfg): tiles on the shifted grid
     static constexpr bool REALIGN = false;         // offset configurations (OCfg): wide boxes realigned per stage
@@ -154,7 +154,8 @@ __device__ __forceinline__ void chain_j(const float *__restrict__ xs, const floa
 //
 // The same loop is spelt three ways because the compiler schedules them differently and each kernel family keeps
 // the spelling it measured fastest with (differences of 1-2% on the large step, 17% on tiny steps):
-//   * a full stage: the inline body under one unroll (tile and slab kernels), or the per-j helper (stream kernel);
+//   * a full stage: the inline body under one unroll (tile and slab kernels), or the per-j helper (stream kernel, and
+//     the tile kernel's rows-outer 8 x 8 configuration);
 //   * a partial stage (the ragged end of C, or the end of a piece in the stream kernel): blocks of four unrolled j,
 //     then one at a time (stream kernel and the small tiles, where C below the stage size makes every stage
 //     partial), or the full-stage loop with a run-time count (the large tiles and the slab kernel, whose full stages
@@ -163,7 +164,7 @@ template <class Cfg, bool FULL>
 __device__ __forceinline__ void chain_block(const float *__restrict__ xs, const float *__restrict__ ds,
                                             const int (&ro)[Cfg::SR], const int (&co)[Cfg::SN],
                                             float (&acc)[Cfg::RM][Cfg::RN], int nj) {
-    constexpr bool kHelper = Cfg::SLAB == 2;
+    constexpr bool kHelper = Cfg::SLAB == 2 || Cfg::ROWS_OUTER;
     constexpr bool kBlocked = Cfg::SLAB == 2 || (Cfg::SLAB == 0 && Cfg::RM * Cfg::RN < 32);
     if constexpr (FULL && kHelper) {
 #pragma unroll(Cfg::UNROLL)
@@ -249,7 +250,7 @@ __device__ __forceinline__ void epilogue(const TmaParams &p, const Tile &tl, con
     }
 }
 
-// The epilogue of a tile stored by TMA (stream kernel, TMID): d_u + acc, one rounding each, written back over the
+// The epilogue of a tile stored by TMA (TMID configurations): d_u + acc, one rounding each, written back over the
 // staged d_u tile us[TI][TC] at the thread's own positions. Rows and columns outside the operands are written too (on
 // zero-filled d_u); the TMA store leaves them out.
 template <class Cfg>
@@ -438,6 +439,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
                     ok = false;
                     break;
                 }
+                if constexpr (Cfg::TMID) {
+                    // the previous tile, written back over the d_u buffer by the consumers: one TMA store, read out of
+                    // the buffer before this tile's d_u box goes into it
+                    const Tile tp = decode_tile<Cfg>(p, t - static_cast<int>(gridDim.x));
+                    dev::tma_store_3d(&p.tm_du, tp.c0, tp.i0, tp.n, base_s + Cfg::OFF_U);
+                    dev::bulk_wait_read_all();
+                }
                 dev::mbar_arrive_expect_tx(du_full, Cfg::DU_TX);
                 dev::tma_load_3d(base_s + Cfg::OFF_U, &p.tm_du, du_x<Cfg>(p, tl), du_y<Cfg>(p, tl), tl.n, du_full);
                 ++du_issued;
@@ -458,6 +466,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             if (du_issued > 0 && !dev::mbar_wait(du_full, static_cast<uint32_t>(du_issued - 1) & 1u, p.timeout_ns))
                 atomicOr(p.err, kErrDrainWait);
         }
+        if constexpr (Cfg::TMID) dev::bulk_wait_all();   // every store performed before the CTA ends
         return;
     }
 
@@ -534,7 +543,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_tma_kernel(const _
             if (lane == 0) atomicOr(p.err, kErrConsumerWait);
             return;
         }
-        epilogue<Cfg>(p, tl, us, ro, co, acc);
+        if (Cfg::TMID && t + static_cast<int>(gridDim.x) < p.ntiles) {
+            // a tile before the CTA's last: back over the d_u buffer, stored by the producer (TMID)
+            epilogue_to_smem<Cfg>(const_cast<float *>(us), ro, co, acc);
+            dev::fence_proxy_async_smem();
+        } else {
+            epilogue<Cfg>(p, tl, us, ro, co, acc);
+        }
         __syncwarp();
         if (lane == 0) dev::mbar_arrive(du_empty);
     }
@@ -1242,7 +1257,18 @@ ConfigInfo info_of() {
 // host's geometry rule: for the larger tiles it is what the configuration reached on a GB300 with every SM busy; for
 // the small latency-oriented tiles it was fitted so that the rule reproduces the measured ordering of small steps.
 using C0 = TCfg<8, 4, 4, 4, 16, 4, 1, 75>;   // 128 x 128, 16 consumer warps, 8 x 4 per thread
-using C1 = TCfg<8, 8, 4, 2, 32, 3, 1, 73>;   // 128 x 128,  8 warps, 8 x 8 per thread
+// The tile kernel's 8 x 8 configuration runs the stream kernel's form of the loop (rows-outer packed FMAs, the per-j
+// helper, an unroll of 16) and stores the tiles a CTA finishes before its last by TMA: the consumers write d_u + acc
+// back over the staged d_u box, and the producer stores it before it loads the next tile's d_u there (with 8 warps the
+// consumers' own stores of a tile take ~1 us). Measured against the plain 8 x 8 / 8 x 4 tile kernels: 23.2 against
+// 24.8 / 23.8 us on 256 x 128 x 128, 61.8 against 67.4 / 65.6 us on 800 x 128 x 128.
+template <class T, int UNROLL_>
+struct TmCfg : T {
+    static constexpr bool ROWS_OUTER = true;
+    static constexpr int UNROLL = UNROLL_;
+    static constexpr bool TMID = true;
+};
+using C1 = TmCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 73>, 16>;   // 128 x 128,  8 warps, 8 x 8 per thread
 using C2 = TCfg<8, 8, 4, 1, 32, 3, 2, 70>;   // 128 x  64,  4 warps
 using C3 = TCfg<8, 8, 2, 2, 32, 3, 2, 70>;   //  64 x 128,  4 warps
 using C4 = TCfg<4, 8, 4, 2, 32, 3, 2, 70>;   //  64 x 128,  8 warps, 4 x 8 per thread
