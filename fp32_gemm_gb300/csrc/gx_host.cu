@@ -249,7 +249,7 @@ constexpr double kMemBytesPerUs = 7.0e6;
 // measured wherever a stream configuration is the fastest (C >= 96: up to 7% faster; at C <= 64, where tile kernels
 // win, between 6% faster and 11% slower); 14's rate is fitted to its own sweep times with the other constants fixed,
 // and so is 1's (the 8 x 8 tile with its TMA stores, above the 8 x 4 tile's 0: faster on 84 of the sweep's 102 shapes)
-constexpr double kRate[] = {0.797, 0.812, 0.749, 0.752, 0.763, 0.721, 0.709, 0.677, 0.433, 0.430, 0.365,
+constexpr double kRate[] = {0.797, 0.812, 0.829, 0.823, 0.763, 0.746, 0.731, 0.677, 0.433, 0.430, 0.365,
                             0.731, 1.000, 0.971, 1.045, 0.590, 0.480, 0.630, 0.305};
 constexpr int kRates = static_cast<int>(sizeof(kRate) / sizeof(kRate[0]));
 }  // namespace model

@@ -1257,23 +1257,29 @@ ConfigInfo info_of() {
 // host's geometry rule: for the larger tiles it is what the configuration reached on a GB300 with every SM busy; for
 // the small latency-oriented tiles it was fitted so that the rule reproduces the measured ordering of small steps.
 using C0 = TCfg<8, 4, 4, 4, 16, 4, 1, 75>;   // 128 x 128, 16 consumer warps, 8 x 4 per thread
-// The tile kernel's 8 x 8 configuration runs the stream kernel's form of the loop (rows-outer packed FMAs, the per-j
-// helper, an unroll of 16) and stores the tiles a CTA finishes before its last by TMA: the consumers write d_u + acc
-// back over the staged d_u box, and the producer stores it before it loads the next tile's d_u there (with 8 warps the
-// consumers' own stores of a tile take ~1 us). Measured against the plain 8 x 8 / 8 x 4 tile kernels: 23.2 against
-// 24.8 / 23.8 us on 256 x 128 x 128, 61.8 against 67.4 / 65.6 us on 800 x 128 x 128.
-template <class T, int UNROLL_>
+// Tile configurations that store the tiles a CTA finishes before its last by TMA: the consumers write d_u + acc back
+// over the staged d_u box, and the producer stores it before it loads the next tile's d_u there. With 8 x 8 thread
+// tiles they also run the stream kernel's form of the loop (rows-outer packed FMAs, the per-j helper, an unroll of 16).
+// Measured on multi-round steps against the same tile without either (us a step):
+//   128 x 128, 8 warps of 8 x 8: 23.2 against 24.8 on 256 x 128 x 128 (the 8 x 4 tile: 23.8), 61.8 against 67.4
+//   (65.6) on 800 x 128 x 128, where the consumers' own stores of a tile take ~1 us;
+//   128 x 64, 4 warps of 8 x 8: 22.8 on 256 x 128 x 128, the fastest tile there (plans without a workspace take it);
+//   64 x 128, 4 warps of 8 x 8: 33.3 against 36.5 on 200 x 192 x 128, 62.2 against 69.7 on 200 x 192 x 256;
+//   64 x 64 and 32 x 128, 4 warps of 4 x 8 (the stores only; the loop form made no difference): 1-5% faster on the
+//   sweep's multi-round shapes (9.0 against 9.2 on 300 x 64 x 96, 30.7 against 32.0 on 600 x 96 x 128), 1% slower on
+//   800 x 32 x 128. The 64 x 128 tile with 8 warps of 4 x 8 measured 2% slower with them and keeps its own stores.
+template <class T, bool RO_, int UNROLL_ = T::UNROLL>
 struct TmCfg : T {
-    static constexpr bool ROWS_OUTER = true;
+    static constexpr bool ROWS_OUTER = RO_;
     static constexpr int UNROLL = UNROLL_;
     static constexpr bool TMID = true;
 };
-using C1 = TmCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 73>, 16>;   // 128 x 128,  8 warps, 8 x 8 per thread
-using C2 = TCfg<8, 8, 4, 1, 32, 3, 2, 70>;   // 128 x  64,  4 warps
-using C3 = TCfg<8, 8, 2, 2, 32, 3, 2, 70>;   //  64 x 128,  4 warps
+using C1 = TmCfg<TCfg<8, 8, 4, 2, 32, 3, 1, 73>, true, 16>;   // 128 x 128,  8 warps, 8 x 8 per thread
+using C2 = TmCfg<TCfg<8, 8, 4, 1, 32, 3, 2, 70>, true, 16>;   // 128 x  64,  4 warps
+using C3 = TmCfg<TCfg<8, 8, 2, 2, 32, 3, 2, 70>, true, 16>;   //  64 x 128,  4 warps
 using C4 = TCfg<4, 8, 4, 2, 32, 3, 2, 70>;   //  64 x 128,  8 warps, 4 x 8 per thread
-using C5 = TCfg<4, 8, 4, 1, 32, 4, 2, 66>;   //  64 x  64,  4 warps
-using C6 = TCfg<4, 8, 2, 2, 32, 4, 2, 66>;   //  32 x 128,  4 warps
+using C5 = TmCfg<TCfg<4, 8, 4, 1, 32, 4, 2, 66>, false>;       //  64 x  64,  4 warps
+using C6 = TmCfg<TCfg<4, 8, 2, 2, 32, 4, 2, 66>, false>;       //  32 x 128,  4 warps
 using C7 = TCfg<4, 4, 2, 2, 32, 2, 4, 60>;   //  32 x  64,  4 warps (latency-bound steps)
 using C8 = TCfg<2, 4, 2, 2, 32, 2, 4, 28>;   //  16 x  64,  4 warps
 using C9 = TCfg<4, 4, 1, 1, 32, 2, 8, 25>;   //  16 x  32,  1 warp
