@@ -116,6 +116,27 @@ def test_every_tma_config_ragged(config):
 GENERIC_CONFIGS = [0, 1, 2, 3]
 
 
+@pytest.mark.parametrize("config", list(range(MAX_TMA_CONFIGS)))
+def test_every_tile_config_multi_round(config):
+    """Every tile configuration forced on a step with more tiles than resident CTAs (400 chunks of 100 x 76: a CTA
+    runs two or more tiles, so the configurations that store the tiles before a CTA's last by TMA do so), ragged in rows
+    and columns, two chained steps, bit-exact against the oracle with the guard bands intact."""
+    if config >= gx.num_configs(1) or gx.config_info(1, config)["kind"] != "tile":
+        pytest.skip("not a tile configuration")
+    w = synth.Workload("multi_round", 66, T=2, P=400, C=100, hd=76, x_scale="inv_sqrt_c")
+    inp = synth.make_inputs(w)
+    want, _ = _oracle_steps(inp, w.P, [1, 0])
+    du, dx, dv = _dev(inp)
+    pl = gx.Plan(du.t, dx.t, dv.t, w.P, flags=gx.config_flag(config))
+    g = pl.geometry()
+    assert g["config"] == config and g["tiles"] > g["ctas"]
+    pl.run(1, -1, pdl=True)
+    torch.cuda.synchronize()
+    assert_bitwise(du.host(), want, f"tile config {config}, {g['tiles']} tiles on {g['ctas']} CTAs")
+    assert du.guards_intact()
+    _check_untouched(dx, dv, inp, f"tile config {config}")
+
+
 def test_generic_menu_covered():
     assert gx.num_configs(0) == len(GENERIC_CONFIGS), "every generic configuration must be in GENERIC_CONFIGS"
 
