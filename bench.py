@@ -500,8 +500,11 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
             others[nm] = measure_chain_workload(gx, nm, args, ws, rank, dev, stream,
                                                 local if ws > 1 else torch.cuda.current_device())
     err = gx.device_error(clear=True)
-    if err:
+    if err & gx.ERR_FATAL_MASK:
         raise RuntimeError(f"device error word {err:#x} after the timed region")
+    # the informational bit: a CTA waited over 1 ms for its neighbour's partial sums and recomputed that tile's chain
+    # (exact results; seen under a profiler's replays, not in plain runs): reported in the line, not fatal
+    handoff_recomputed = bool(err & gx.ERR_HANDOFF_RECOMPUTED)
 
     # e2e: host buffers through the public API (sdm_gx_gemm_plan_run_host: the T steps fed from pinned host memory, each
     # step's copies in overlapped with the previous step's compute, each step's d_u copied back), all inside the timed
@@ -591,6 +594,7 @@ def run_ours(args, w: synth.Workload, ws: int, rank: int, local: int) -> dict:
                          "pinned host -> device copies, the chain's graph, d_u back to pinned host")},
         "gpu_launches": launches,
         "clocks": clocks,
+        **({"handoff_recomputed": True} if handoff_recomputed else {}),
         **({"other_workloads": others} if others else {}),
     }
     return out

@@ -10,7 +10,7 @@ ctypes binding. PyTorch provides device memory and streams only.
 from ._binding import (FLAG_CONFIG_MASK, FLAG_CTAS_SHIFT, FLAG_GENERIC, FLAG_NO_PREFETCH, Geom, Graph, GxGemmError, Plan,  # noqa: F401,E501
                        Strides, abi_version, device_error, geometry, kernel_attrs, launch_counts, lib, num_configs,
                        producer_step, step, step_ex, strerror)
-from ._binding import (FLAG_NOALLOC, FLAG_TEST_NO_HANDOFF, FLAG_TEST_STALL, FLAG_X_TRANSPOSED, LIB_PATH, autotune, choose_config, config_info,  # noqa: F401
+from ._binding import (ERR_FATAL_MASK, ERR_HANDOFF_RECOMPUTED, FLAG_NOALLOC, FLAG_TEST_NO_HANDOFF, FLAG_TEST_STALL, FLAG_X_TRANSPOSED, LIB_PATH, autotune, choose_config, config_info,  # noqa: F401
                        noalloc_geometry, step_noalloc, stream_pieces, workspace_size)
 
 

@@ -24,6 +24,11 @@ FLAG_NOALLOC = 0x800   # geometry(): the launch sdm_gx_gemm_step_noalloc would m
 FLAG_X_TRANSPOSED = 0x10000   # x stored [n][i][j] (passed here as a transpose(1, 2) view; set automatically)
 FLAG_CONFIG_MASK = 0x0FF
 FLAG_CTAS_SHIFT = 12
+FLAG_CTAS_MASK = 0xF000
+
+# bits of the device error word (sdm_gx_device_error)
+ERR_FATAL_MASK = 0x7              # bits 0-2: a kernel gave up a bounded wait, its step is incomplete
+ERR_HANDOFF_RECOMPUTED = 0x8      # bit 3, informational: a tile's chain recomputed after a late hand-off (exact)
 
 STATUS = {
     0: "SDM_GX_OK", -1: "SDM_GX_E_NULL", -2: "SDM_GX_E_SHAPE", -3: "SDM_GX_E_RANGE", -4: "SDM_GX_E_ALIGN",

@@ -17,6 +17,10 @@
 #include "gx_internal.h"
 #include "sdm_gx_gemm.h"
 
+static_assert(sdmgx::kErrFatalMask == SDM_GX_ERR_FATAL_MASK &&
+                  sdmgx::kErrHandoffRecomputed == SDM_GX_ERR_HANDOFF_RECOMPUTED,
+              "the device error word's bits as the header documents them");
+
 // The device error word: bits of sdmgx::kErr* set by kernels whose bounded waits expired. One word per device (each
 // device's module instance has its own copy); its device address is looked up once per device.
 __device__ uint32_t g_sdm_gx_error_word;

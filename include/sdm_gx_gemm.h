@@ -389,6 +389,8 @@ SDM_GX_API int sdm_gx_gemm_num_configs(int32_t path);
  * tile's whole chain itself, so the step's results are exact (the call returns SDM_GX_OK). Synchronizes the device.
  * clear != 0 resets the word to 0 afterwards. */
 SDM_GX_API int sdm_gx_device_error(uint32_t *word, int clear);
+#define SDM_GX_ERR_FATAL_MASK         0x7u   /* bits 0-2: a bounded wait gave up, the step is incomplete            */
+#define SDM_GX_ERR_HANDOFF_RECOMPUTED 0x8u   /* bit 3, informational: a tile's chain recomputed, results exact      */
 
 /* Launches of the library's kernels since load (the page's PDL_LAUNCHES counters, split by kernel): out[0] = step
  * kernels, out[1] = producer kernels,

@@ -28,6 +28,15 @@ def test_exports_every_declared_symbol():
     assert set(names) == set(gx._binding.SIGNATURES), "binding signatures and header declarations differ"
 
 
+def test_header_constants_match_binding():
+    """Every flag and error-word bit the header defines has the same value in the Python binding."""
+    src = open(HEADER).read()
+    defs = re.findall(r"#define SDM_GX_((?:FLAG|ERR)_\w+)\s+(0x[0-9A-Fa-f]+|\d+)u?\b", src)
+    assert len(defs) >= 10
+    for name, value in defs:
+        assert getattr(gx._binding, name) == int(value, 0), name
+
+
 def test_version_and_strerror():
     assert gx.abi_version() == 1
     for code, name in gx._binding.STATUS.items():
