@@ -105,23 +105,25 @@ struct Pieces {
 // unit u of the step at cost u + kappa * floor(u / C) (every tile begun after the first costs kappa units more) back
 // from a cost y: inside tile t the cost runs t (C + kappa) .. t (C + kappa) + C; the kappa after it maps to the
 // tile's end
-__host__ __device__ inline int64_t unit_at_cost(int64_t y, int C, int kappa) {
-    const int64_t t = y / (C + kappa);
-    const int64_t r = y - t * (C + kappa);
+template <class I>
+__host__ __device__ inline I unit_at_cost(I y, I C, I kappa) {
+    const I t = y / (C + kappa);
+    const I r = y - t * (C + kappa);
     return t * C + (r < C ? r : C);
 }
 
-__host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G, int kappa = 0) {
-    // CTA b takes the units between costs b F / G and (b + 1) F / G, F = the step's total cost: with kappa = 0 equal
-    // ranges of units; with kappa > 0 a range that holds a tile boundary (one more piece) holds kappa fewer units
-    const int64_t F = static_cast<int64_t>(ntiles) * (C + kappa) - kappa;   // no charge after the last tile
-    const int64_t lo = unit_at_cost(static_cast<int64_t>(b) * F / G, C, kappa);
-    const int64_t hi = unit_at_cost(static_cast<int64_t>(b + 1) * F / G, C, kappa);
+// CTA b takes the units between costs b F / G and (b + 1) F / G, F = the step's total cost: with kappa = 0 equal
+// ranges of units; with kappa > 0 a range that holds a tile boundary (one more piece) holds kappa fewer units
+template <class I>
+__host__ __device__ inline Pieces cta_pieces_in(I ntiles, I C, I b, I G, I kappa) {
+    const I F = ntiles * (C + kappa) - kappa;   // no charge after the last tile
+    const I lo = unit_at_cost<I>(b * F / G, C, kappa);
+    const I hi = unit_at_cost<I>((b + 1) * F / G, C, kappa);
     Pieces R;
     R.ta = static_cast<int>(lo / C);
-    R.ja = static_cast<int>(lo - static_cast<int64_t>(R.ta) * C);
+    R.ja = static_cast<int>(lo - static_cast<I>(R.ta) * C);
     R.tb = static_cast<int>((hi - 1) / C);
-    R.je = static_cast<int>(hi - static_cast<int64_t>(R.tb) * C);
+    R.je = static_cast<int>(hi - static_cast<I>(R.tb) * C);
     R.has_tail = R.ja > 0 ? 1 : 0;
     R.has_head = R.je < C ? 1 : 0;
     R.first_full = R.has_tail ? R.ta + 1 : R.ta;
@@ -129,6 +131,15 @@ __host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G, in
     R.nfull = last_full >= R.first_full ? last_full - R.first_full + 1 : 0;
     R.count = R.has_head + R.nfull + R.has_tail;
     return R;
+}
+
+// In 32-bit arithmetic wherever G F fits: every thread of a stream-kernel CTA waits for this split before the first
+// copy goes out, and on the large step the 64-bit divisions cost 0.25 us of each step (the CTAs that become resident
+// last start on the critical path).
+__host__ __device__ inline Pieces cta_pieces(int ntiles, int C, int b, int G, int kappa = 0) {
+    const int64_t F = static_cast<int64_t>(ntiles) * (C + kappa) - kappa;
+    if (F * G <= INT32_MAX) return cta_pieces_in<int32_t>(ntiles, C, b, G, kappa);
+    return cta_pieces_in<int64_t>(ntiles, C, b, G, kappa);
 }
 
 // The split's charge per tile boundary (units of (tile, j)): a CTA whose range holds one more boundary runs one more

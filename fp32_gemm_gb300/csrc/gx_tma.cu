@@ -950,8 +950,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) gx_stream_kernel(cons
         dev::mbar_init(epoch_known, 1);
         dev::mbar_init(tile_staged, Cfg::NCW);
         dev::fence_mbar_init();
-        *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G, p.stream_kappa);
     }
+    // the CTA's range, decoded by another warp while thread 0 sets up the barriers (both sit before the first copy)
+    if (vt == 32) *reinterpret_cast<Pieces *>(base_g + Cfg::OFF_PIECES) = cta_pieces(p.ntiles, p.C, b, G, p.stream_kappa);
     __syncthreads();
     if (vt == 0) trace_at(p, 0);
     // read from shared memory where needed, so that no thread keeps the descriptor in registers

@@ -91,3 +91,21 @@ def test_stream_split_rejects_short_ranges():
         gx.stream_pieces(100, 128, 152, 0)      # fewer tiles than CTAs: a range would be shorter than a tile
     with pytest.raises(gx.GxGemmError):
         gx.stream_pieces(256, 128, 152, 152)    # no such CTA
+
+
+@pytest.mark.parametrize("ntiles", [100_900, 100_915, 100_916, 101_000, 2_000_000, 16_000_000])
+def test_stream_split_on_both_sides_of_32_bit_arithmetic(ntiles):
+    """The split is computed in 32-bit arithmetic while G x F fits in 31 bits (F = ntiles (C + KAPPA) - KAPPA, the
+    step's cost) and in 64-bit beyond: both give the ranges of the cost formula, here in Python integers."""
+    C, G = 128, 152
+    F = ntiles * (C + KAPPA) - KAPPA
+
+    def unit_at_cost(y):
+        t, r = divmod(y, C + KAPPA)
+        return t * C + min(r, C)
+
+    for b in (0, 1, 75, 150, 151):
+        pcs = gx.stream_pieces(ntiles, C, G, b)
+        lo = min(t * C + j0 for (t, j0, _, _) in pcs)
+        hi = max(t * C + j1 for (t, _, j1, _) in pcs)
+        assert (lo, hi) == (unit_at_cost(b * F // G), unit_at_cost((b + 1) * F // G)), (ntiles, b)
